@@ -1,0 +1,156 @@
+"""fp64 CPU oracle for the selective scan (S6) and its decode update.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
+CPU-baseline leg are the only callers. The CUDA library never imports it and
+shares no code with it.
+
+The arithmetic lives in ss_oracle.c (plain C, fp64, sequential in time); this
+module compiles it with gcc (no fast-math) and wraps it with ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ss_oracle.c")
+_LIB = os.path.join(_HERE, "libss_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ss_oracle.c into libss_oracle.so (gcc -O2, IEEE semantics)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC",
+                               "-shared", "-o", tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P, I, LL, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_double
+        lib.ss_oracle_scan.argtypes = [LL, P, P, I, I, LL, I, P, P, P, P, P, P, P, P, I, P, P, P, I]
+        lib.ss_oracle_scan.restype = I
+        lib.ss_oracle_state_update.argtypes = [LL, P, P, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I]
+        lib.ss_oracle_state_update.restype = I
+        lib.ss_oracle_softplus.argtypes = [D]
+        lib.ss_oracle_softplus.restype = D
+        lib.ss_oracle_silu.argtypes = [D]
+        lib.ss_oracle_silu.restype = D
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _cpu_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return 1
+    if a.dtype == np.float32:
+        return 0
+    raise TypeError("oracle inputs are float32 or bf16 bit patterns (uint16), got %s" % a.dtype)
+
+
+def softplus(x: float) -> float:
+    return _load().ss_oracle_softplus(float(x))
+
+
+def silu(x: float) -> float:
+    return _load().ss_oracle_silu(float(x))
+
+
+def scan_fwd(u, delta, A, B, C, D=None, delta_bias=None, z=None, delta_softplus=True,
+             h0=None, rows=None, dim=None, threads=None):
+    """Selective scan forward in fp64.
+
+    Full-tensor form: u, delta, z of shape (batch, dim, L); B, C (batch, N, L).
+    Row-subset form: pass rows (flat row indices b*dim+d) and dim; u, delta, z
+    are then (len(rows), L) holding just those rows.
+    A is (dim, N) float32; D and delta_bias (dim,) float32 or None.
+    Inputs are float32, or uint16 bf16 bit patterns (all of one kind).
+    h0: None (zero state) or (rows..., N).
+    Returns (y, h_last) in float64, shaped like u and (rows..., N)."""
+    u = np.ascontiguousarray(u)
+    full = rows is None
+    B = np.ascontiguousarray(B)
+    batch, N, L = B.shape
+    if full:
+        batch_u, dim, L_u = u.shape
+        assert batch_u == batch and L_u == L
+        rows = np.arange(batch * dim)
+    else:
+        assert dim is not None
+        rows = np.asarray(rows, dtype=np.int64)
+    nrows = len(rows)
+    code = _dtype_code(u)
+    flat = lambda a: None if a is None else np.ascontiguousarray(a).reshape(nrows, L)
+    u2, d2, z2 = flat(u), flat(delta), flat(z)
+    for a in (d2, z2, B, C):
+        if a is not None and _dtype_code(a) != code:
+            raise TypeError("mixed input dtypes")
+    row_b = (rows // dim).astype(np.int32)
+    row_d = (rows % dim).astype(np.int32)
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    assert A.shape == (dim, N)
+    Dp = None if D is None else np.ascontiguousarray(D, dtype=np.float32)
+    bp = None if delta_bias is None else np.ascontiguousarray(delta_bias, dtype=np.float32)
+    h0p = None if h0 is None else np.ascontiguousarray(h0, dtype=np.float64).reshape(nrows, N)
+    y = np.empty((nrows, L), dtype=np.float64)
+    hl = np.empty((nrows, N), dtype=np.float64)
+    C = np.ascontiguousarray(C)
+    rc = _load().ss_oracle_scan(nrows, _ptr(row_b), _ptr(row_d), dim, N, L, code, _ptr(u2),
+                                _ptr(d2), _ptr(z2), _ptr(A), _ptr(B), _ptr(C), _ptr(Dp),
+                                _ptr(bp), int(bool(delta_softplus)), _ptr(h0p), _ptr(y), _ptr(hl),
+                                threads or _cpu_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    if full:
+        return y.reshape(batch, dim, L), hl.reshape(batch, dim, N)
+    return y, hl
+
+
+def state_update(state, x, dt, A, B, C, D=None, dt_bias=None, z=None, dt_softplus=True,
+                 rows=None, dim=None, threads=None):
+    """One decode step in fp64. state (batch, dim, N) float64 is updated in
+    place; x, dt, z are (batch, dim) (or (len(rows),) with rows/dim given);
+    B, C are (batch, N). Returns y (float64) shaped like x."""
+    B = np.ascontiguousarray(B)
+    batch, N = B.shape
+    if rows is None:
+        dim = x.shape[1]
+        rows = np.arange(batch * dim)
+    rows = np.asarray(rows, dtype=np.int64)
+    nrows = len(rows)
+    assert state.dtype == np.float64 and state.flags.c_contiguous and state.size == nrows * N
+    code = _dtype_code(np.asarray(x))
+    row_b = (rows // dim).astype(np.int32)
+    row_d = (rows % dim).astype(np.int32)
+    cont = lambda a: None if a is None else np.ascontiguousarray(a)
+    x, dt, z, C = cont(x), cont(dt), cont(z), cont(C)
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    Dp = None if D is None else np.ascontiguousarray(D, dtype=np.float32)
+    bp = None if dt_bias is None else np.ascontiguousarray(dt_bias, dtype=np.float32)
+    y = np.empty(nrows, dtype=np.float64)
+    rc = _load().ss_oracle_state_update(nrows, _ptr(row_b), _ptr(row_d), dim, N, code,
+                                        _ptr(state), _ptr(x), _ptr(dt), _ptr(z), _ptr(A),
+                                        _ptr(B), _ptr(C), _ptr(Dp), _ptr(bp),
+                                        int(bool(dt_softplus)), _ptr(y), threads or 1)
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return y.reshape(np.asarray(x).shape)

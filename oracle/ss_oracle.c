@@ -1,0 +1,181 @@
+/*
+ * Plain fp64 CPU oracle of the selective scan (S6) forward pass and of the
+ * single-token decode state update.
+ *
+ * TEST INFRASTRUCTURE ONLY. It exists to check the CUDA library; only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg may load it. It
+ * shares no code, header or table with the CUDA path.
+ *
+ * What it computes, per row (b, d) of the (batch, dim) grid, sequentially in l:
+ *
+ *   x      = delta[b,d,l] + bias[d]
+ *   dt     = softplus(x)                    (or x itself when softplus is off)
+ *   for n:  h[n] = exp(dt * A[d,n]) * h[n] + dt * B[b,n,l] * u[b,d,l]
+ *   y      = sum_n C[b,n,l] * h[n] + D[d] * u[b,d,l]
+ *   y     *= z * sigmoid(z)                 (when z is given)
+ *   h_last[b,d,:] = h after the last step
+ *
+ * Sources, by page title and section:
+ *  - "Mamba: Linear-Time Sequence Modeling with Selective State Spaces",
+ *    section "Method": zero-order-hold discretisation, A_bar = exp(Delta A),
+ *    and the recurrence h_t = A_bar h_{t-1} + B_bar x_t, y_t = C h_t.
+ *  - same page, section "The Selection Mechanism (S6)": B_t and C_t are
+ *    per-token projections of width N (shared by every channel d) and
+ *    Delta_t = softplus(parameter + projection).
+ *  - soft186.com, "Mamba选择性状态空间机制", section "动态参数化的状态空间": the
+ *    step is dt = softplus(projection + delta_bias), dA = exp(dt * A), and the
+ *    state update multiplies the state by dA and adds the input times dt*B
+ *    (the simplified input matrix dt*B is used instead of the exact ZOH B_bar).
+ *  - same Mamba page, section "Key terms" (Mamba block): a multiplicative
+ *    gate follows the SSM; it is silu(z) here and multiplies C.h + D*u.
+ *  - same Mamba page, section "Questions": decoding keeps only the fixed-size
+ *    D x N state per layer and advances it by one step per token.
+ *
+ * Inputs are read exactly (fp32 as is, bf16 bit patterns widened exactly) and
+ * all arithmetic is fp64 with the C library's exp and log1p.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_F32 = 0, ORC_BF16 = 1 };
+
+static double rd(const void *p, long long i, int dtype) {
+    if (dtype == ORC_BF16) {
+        uint32_t bits = ((uint32_t)((const uint16_t *)p)[i]) << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float *)p)[i];
+}
+
+/* softplus(x) = log(1 + e^x), evaluated without overflow or cancellation. */
+double ss_oracle_softplus(double x) {
+    return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
+double ss_oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+typedef struct {
+    /* geometry */
+    long long nrows, seqlen;
+    int dim, dstate, dtype;
+    const int *row_b, *row_d;          /* (nrows): batch and channel of each row */
+    /* inputs */
+    const void *u, *delta, *z;         /* (nrows, seqlen); z may be NULL */
+    const float *A;                    /* (dim, dstate) */
+    const void *B, *C;                 /* (batch, dstate, seqlen) */
+    const float *D, *bias;             /* (dim); may be NULL */
+    int softplus;
+    const double *h0;                  /* (nrows, dstate) or NULL */
+    /* outputs */
+    double *y;                         /* (nrows, seqlen) or NULL */
+    double *h_last;                    /* (nrows, dstate) or NULL */
+    /* work split */
+    long long lo, hi;
+} scan_job;
+
+static void scan_rows(const scan_job *j) {
+    const long long L = j->seqlen;
+    const int N = j->dstate;
+    double *h = (double *)malloc(sizeof(double) * (size_t)N);
+    for (long long r = j->lo; r < j->hi; ++r) {
+        const int b = j->row_b[r], d = j->row_d[r];
+        const long long urow = r * L;
+        const long long bcrow = (long long)b * N * L;
+        for (int n = 0; n < N; ++n) h[n] = j->h0 ? j->h0[r * N + n] : 0.0;
+        const double bias = j->bias ? (double)j->bias[d] : 0.0;
+        const double Dd = j->D ? (double)j->D[d] : 0.0;
+        for (long long l = 0; l < L; ++l) {
+            const double uv = rd(j->u, urow + l, j->dtype);
+            const double x = rd(j->delta, urow + l, j->dtype) + bias;
+            const double dt = j->softplus ? ss_oracle_softplus(x) : x;
+            double yv = 0.0;
+            for (int n = 0; n < N; ++n) {
+                const double a = (double)j->A[(long long)d * N + n];
+                const double Bv = rd(j->B, bcrow + (long long)n * L + l, j->dtype);
+                const double Cv = rd(j->C, bcrow + (long long)n * L + l, j->dtype);
+                h[n] = exp(dt * a) * h[n] + dt * Bv * uv;
+                yv += Cv * h[n];
+            }
+            yv += Dd * uv;
+            if (j->z) yv *= ss_oracle_silu(rd(j->z, urow + l, j->dtype));
+            if (j->y) j->y[urow + l] = yv;
+        }
+        if (j->h_last)
+            for (int n = 0; n < N; ++n) j->h_last[r * N + n] = h[n];
+    }
+    free(h);
+}
+
+static void *scan_thread(void *arg) {
+    scan_rows((const scan_job *)arg);
+    return NULL;
+}
+
+/*
+ * Selective scan forward over an explicit list of rows.
+ *
+ * row_b/row_d give the (batch, channel) of each of the nrows rows; u, delta
+ * and z hold those rows only, row-major (nrows, seqlen). B and C hold every
+ * batch, (batch, dstate, seqlen). dtype: 0 = fp32, 1 = bf16 bit patterns.
+ * h0 (nrows, dstate) or NULL for a zero initial state. y (nrows, seqlen) and
+ * h_last (nrows, dstate) are written in fp64; either may be NULL.
+ * nthreads <= 0 uses one thread. Returns 0, or -1 on a bad argument.
+ */
+int ss_oracle_scan(long long nrows, const int *row_b, const int *row_d, int dim,
+                   int dstate, long long seqlen, int dtype, const void *u,
+                   const void *delta, const void *z, const float *A, const void *B,
+                   const void *C, const float *D, const float *delta_bias,
+                   int delta_softplus, const double *h0, double *y, double *h_last,
+                   int nthreads) {
+    if (nrows < 0 || dim <= 0 || dstate <= 0 || seqlen < 0) return -1;
+    if (!row_b || !row_d || !u || !delta || !A || !B || !C) return -1;
+    if (dtype != ORC_F32 && dtype != ORC_BF16) return -1;
+    for (long long r = 0; r < nrows; ++r)
+        if (row_d[r] < 0 || row_d[r] >= dim || row_b[r] < 0) return -1;
+    scan_job base = {nrows, seqlen, dim, dstate, dtype, row_b, row_d, u, delta, z,
+                     A, B, C, D, delta_bias, delta_softplus, h0, y, h_last, 0, nrows};
+    if (nthreads <= 1 || nrows < 2) {
+        scan_rows(&base);
+        return 0;
+    }
+    if (nthreads > nrows) nthreads = (int)nrows;
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    scan_job *jobs = (scan_job *)malloc(sizeof(scan_job) * (size_t)nthreads);
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = base;
+        jobs[t].lo = nrows * t / nthreads;
+        jobs[t].hi = nrows * (t + 1) / nthreads;
+        pthread_create(&tid[t], NULL, scan_thread, &jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t) pthread_join(tid[t], NULL);
+    free(jobs);
+    free(tid);
+    return 0;
+}
+
+/*
+ * Decode: one token per row. The state (nrows, dstate) is read and replaced
+ * by the state after the step; y (nrows) receives the gated output. x, dt, z
+ * are (nrows); B, C are (batch, dstate). This is the scan above with one
+ * time step and h0 = state.
+ */
+int ss_oracle_state_update(long long nrows, const int *row_b, const int *row_d,
+                           int dim, int dstate, int dtype, double *state,
+                           const void *x, const void *dt, const void *z,
+                           const float *A, const void *B, const void *C,
+                           const float *D, const float *dt_bias, int dt_softplus,
+                           double *y, int nthreads) {
+    if (!state) return -1;
+    double *h_new = (double *)malloc(sizeof(double) * (size_t)(nrows * dstate + 1));
+    int rc = ss_oracle_scan(nrows, row_b, row_d, dim, dstate, 1, dtype, x, dt, z, A,
+                            B, C, D, dt_bias, dt_softplus, state, y, h_new, nthreads);
+    if (rc == 0) memcpy(state, h_new, sizeof(double) * (size_t)(nrows * dstate));
+    free(h_new);
+    return rc;
+}

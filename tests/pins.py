@@ -1,0 +1,298 @@
+"""Closed forms and invariants that pin the fp64 oracle to the mathematics.
+
+None of these re-types the oracle's sequential recurrence: each reaches the
+same numbers by another road (a materialised sum over all past inputs, a
+convolution kernel, a gate identity, a limit), so that a dropped term, a wrong
+sign, a wrong index or a transposed operand in the oracle shows up as a
+mismatch. Sources, by page title and section:
+  "Mamba: Linear-Time Sequence Modeling with Selective State Spaces"
+    - "Method": ZOH discretisation A_bar = exp(Delta A); recurrence.
+    - "The Selection Mechanism (S6)": input-dependent B, C, Delta; with N = 1,
+      A = -1, B = 1 the recurrence is a classical gated RNN update.
+    - "Key terms" / "Questions": LTI systems are convolutions; a small Delta
+      keeps the state and ignores the input; the parallel associative scan.
+  soft186.com "Mamba选择性状态空间机制", "动态参数化的状态空间": dt = softplus(
+    projection + bias), dA = exp(dt A), state = state * dA + x * dt * B.
+Every function takes an `orc` object exposing scan_fwd / state_update with the
+signature of the `oracle` module, and returns the max error it found.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def softplus_ref(x):
+    # numpy's log(e^0 + e^x): a library route distinct from the oracle's C code
+    return np.logaddexp(0.0, x)
+
+
+def silu_ref(z):
+    # z * sigmoid(z) with sigmoid written through tanh
+    return z * 0.5 * (1.0 + np.tanh(0.5 * z))
+
+
+def small_case(seed=0, batch=2, dim=3, N=4, L=40, softplus=True, with_z=True, with_D=True,
+               with_bias=True, with_h0=False):
+    g = np.random.default_rng(seed)
+    f = lambda *s: g.standard_normal(s).astype(np.float32)
+    case = dict(u=f(batch, dim, L), delta=f(batch, dim, L), B=f(batch, N, L), C=f(batch, N, L),
+                A=-(g.uniform(0.2, 2.0, (dim, N))).astype(np.float32),
+                D=f(dim) if with_D else None,
+                delta_bias=(g.uniform(-3.0, 0.5, dim)).astype(np.float32) if with_bias else None,
+                z=f(batch, dim, L) if with_z else None, delta_softplus=softplus,
+                h0=f(batch, dim, N).astype(np.float64) if with_h0 else None)
+    return case
+
+
+def materialised_scan(c):
+    """y and every state h_t from the unrolled sum
+        h_t[n] = exp(A[n] S_t) h0[n] + sum_{s<=t} exp(A[n](S_t - S_s)) dt_s B_s[n] u_s,
+    S_t = dt_0 + ... + dt_t, which is the recurrence with all products of
+    exp(dt A) collapsed into one exponential of a sum. O(L^2 N) work."""
+    u = c["u"].astype(np.float64)
+    batch, dim, L = u.shape
+    B = c["B"].astype(np.float64)
+    C = c["C"].astype(np.float64)
+    A = c["A"].astype(np.float64)
+    x = c["delta"].astype(np.float64)
+    if c.get("delta_bias") is not None:
+        x = x + c["delta_bias"].astype(np.float64)[None, :, None]
+    dt = softplus_ref(x) if c.get("delta_softplus", True) else x
+    S = np.cumsum(dt, axis=-1)                                  # (b, d, t)
+    diff = S[:, :, :, None] - S[:, :, None, :]                 # (b, d, t, s)
+    causal = np.tril(np.ones((L, L), dtype=bool))
+    W = np.exp(A[None, :, :, None, None] * diff[:, :, None, :, :])
+    W = np.where(causal[None, None, None], W, 0.0)              # (b, d, n, t, s)
+    drive = dt * u                                              # (b, d, s)
+    H = np.einsum("bdnts,bns,bds->bdnt", W, B, drive)
+    if c.get("h0") is not None:
+        H = H + np.exp(A[None, :, :, None] * S[:, :, None, :]) * c["h0"][:, :, :, None]
+    y = np.einsum("bnt,bdnt->bdt", C, H)
+    if c.get("D") is not None:
+        y = y + c["D"].astype(np.float64)[None, :, None] * u
+    if c.get("z") is not None:
+        y = y * silu_ref(c["z"].astype(np.float64))
+    return y, H
+
+
+def run(orc, c, **over):
+    kw = dict(c)
+    kw.update(over)
+    return orc.scan_fwd(kw["u"], kw["delta"], kw["A"], kw["B"], kw["C"], D=kw.get("D"),
+                        delta_bias=kw.get("delta_bias"), z=kw.get("z"),
+                        delta_softplus=kw.get("delta_softplus", True), h0=kw.get("h0"))
+
+
+def rel_err(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.max(np.abs(a - b)) / max(1.0, float(np.max(np.abs(b)))))
+
+
+# ---- individual pins ----------------------------------------------------------------
+
+def pin_materialised(orc, **case_kw):
+    """Time-varying inputs: recurrence == unrolled sum (y and h_last)."""
+    c = small_case(**case_kw)
+    y, hl = run(orc, c)
+    y_ref, H = materialised_scan(c)
+    return max(rel_err(y, y_ref), rel_err(hl, H[..., -1]))
+
+
+def pin_lti_convolution(orc, seed=1, dim=2, N=3, L=48):
+    """Constant dt, B, C along time: y = K * u + D u with the convolution
+    kernel K_i = sum_n C_n dA_n^i dt B_n (LTI systems are convolutions)."""
+    g = np.random.default_rng(seed)
+    batch = 1
+    u = g.standard_normal((batch, dim, L)).astype(np.float32)
+    dconst = g.standard_normal(dim).astype(np.float32)
+    delta = np.repeat(dconst[None, :, None], L, axis=2).astype(np.float32)
+    Bn = g.standard_normal(N).astype(np.float32)
+    Cn = g.standard_normal(N).astype(np.float32)
+    B = np.repeat(Bn[None, :, None], L, axis=2).astype(np.float32)
+    C = np.repeat(Cn[None, :, None], L, axis=2).astype(np.float32)
+    A = -(g.uniform(0.1, 1.5, (dim, N))).astype(np.float32)
+    D = g.standard_normal(dim).astype(np.float32)
+    bias = g.uniform(-2, 0, dim).astype(np.float32)
+    y, _ = orc.scan_fwd(u, delta, A, B, C, D=D, delta_bias=bias, z=None)
+    err = 0.0
+    for d in range(dim):
+        dt = float(softplus_ref(np.float64(dconst[d]) + np.float64(bias[d])))
+        dA = np.exp(dt * A[d].astype(np.float64))                     # (N,)
+        i = np.arange(L)
+        K = (Cn.astype(np.float64)[None, :] * dA[None, :] ** i[:, None]
+             * dt * Bn.astype(np.float64)[None, :]).sum(axis=1)         # (L,)
+        uu = u[0, d].astype(np.float64)
+        yref = np.convolve(uu, K)[:L] + float(D[d]) * uu
+        err = max(err, rel_err(y[0, d], yref))
+    return err
+
+
+def pin_single_step(orc, seed=2):
+    """L = 1 from a zero state: h = dt B u, y = (C.h + D u) silu(z)."""
+    c = small_case(seed=seed, L=1)
+    y, hl = run(orc, c)
+    x = c["delta"][..., 0].astype(np.float64) + c["delta_bias"].astype(np.float64)[None]
+    dt = softplus_ref(x)                                              # (b, d)
+    u = c["u"][..., 0].astype(np.float64)
+    h = dt[:, :, None] * c["B"][:, None, :, 0].astype(np.float64) * u[:, :, None]
+    yref = (np.einsum("bn,bdn->bd", c["C"][..., 0].astype(np.float64), h)
+            + c["D"].astype(np.float64)[None] * u) * silu_ref(c["z"][..., 0].astype(np.float64))
+    return max(rel_err(y[..., 0], yref), rel_err(hl, h))
+
+
+def pin_zero_input(orc, seed=3):
+    """u = 0 and h0 = 0: the state and the output stay exactly zero."""
+    c = small_case(seed=seed)
+    c["u"] = np.zeros_like(c["u"])
+    y, hl = run(orc, c)
+    return float(max(np.max(np.abs(y)), np.max(np.abs(hl))))
+
+
+def pin_gated_rnn(orc, seed=4, L=50):
+    """N = 1, A = -1, B = C = 1, D = 0, no gate: exp(-softplus(x)) = 1 - sigmoid(x),
+    so h_t = (1 - g_t) h_{t-1} + dt_t u_t with g_t = sigmoid(x_t)."""
+    g = np.random.default_rng(seed)
+    u = g.standard_normal((1, 1, L)).astype(np.float32)
+    delta = g.standard_normal((1, 1, L)).astype(np.float32)
+    ones = np.ones((1, 1, L), dtype=np.float32)
+    A = -np.ones((1, 1), dtype=np.float32)
+    y, hl = orc.scan_fwd(u, delta, A, ones, ones, D=None, delta_bias=None, z=None)
+    x = delta[0, 0].astype(np.float64)
+    gate = 1.0 / (1.0 + np.exp(-x))
+    dt = softplus_ref(x)
+    h = 0.0
+    href = np.empty(L)
+    for t in range(L):
+        h = (1.0 - gate[t]) * h + dt[t] * float(u[0, 0, t])
+        href[t] = h
+    return max(rel_err(y[0, 0], href), rel_err(hl[0, 0, 0], href[-1]))
+
+
+def pin_geometric_decay(orc, seed=5, l0=20):
+    """Input switched off from l0 on: h_last = exp(A * sum_{s>=l0} dt_s) h_{l0-1},
+    and |h| never grows while the input is off (A < 0)."""
+    c = small_case(seed=seed, with_z=False)
+    L = c["u"].shape[-1]
+    c["u"][..., l0:] = 0.0
+    _, h_prefix = run(orc, {**c, "u": c["u"][..., :l0], "delta": c["delta"][..., :l0],
+                           "B": c["B"][..., :l0], "C": c["C"][..., :l0]})
+    _, hl = run(orc, c)
+    x = c["delta"].astype(np.float64) + c["delta_bias"].astype(np.float64)[None, :, None]
+    Ssum = softplus_ref(x)[..., l0:].sum(axis=-1)                      # (b, d)
+    href = np.exp(c["A"].astype(np.float64)[None] * Ssum[..., None]) * h_prefix
+    err = rel_err(hl, href)
+    # monotone decay through the tail
+    prev = np.abs(h_prefix)
+    for t in range(l0 + 1, L + 1, 5):
+        _, ht = run(orc, {**c, "u": c["u"][..., :t], "delta": c["delta"][..., :t],
+                         "B": c["B"][..., :t], "C": c["C"][..., :t]})
+        if np.any(np.abs(ht) > prev * (1 + 1e-12) + 1e-300):
+            err = max(err, 1.0)
+        prev = np.abs(ht)
+    return err
+
+
+def pin_small_delta(orc, seed=6):
+    """bias -> -30 gives dt ~ e^-30: the state keeps h0 and ignores the input."""
+    c = small_case(seed=seed, with_h0=True, L=64)
+    c["delta_bias"] = np.full(c["A"].shape[0], -30.0, dtype=np.float32)
+    c["delta"] = np.clip(c["delta"], -1.0, 1.0)
+    _, hl = run(orc, c)
+    return float(np.max(np.abs(hl - c["h0"])))
+
+
+def pin_chunk_split(orc, seed=7, L1=17):
+    """Scanning [0, L) equals scanning [0, L1) then [L1, L) from h_{L1}."""
+    c = small_case(seed=seed, with_h0=True)
+    y, hl = run(orc, c)
+    sl = lambda a, s: a[..., s]
+    first = {**c, **{k: sl(c[k], slice(0, L1)) for k in ("u", "delta", "B", "C", "z")}}
+    second = {**c, **{k: sl(c[k], slice(L1, None)) for k in ("u", "delta", "B", "C", "z")}}
+    y1, h1 = run(orc, first)
+    second["h0"] = h1
+    y2, h2 = run(orc, second)
+    return max(rel_err(np.concatenate([y1, y2], axis=-1), y), rel_err(h2, hl))
+
+
+def pin_associative_scan(orc, seed=8, chunkings=((1,), (3,), (16,), (5, 11, 2, 9))):
+    """The final state is the fold of per-step affine maps h -> a h + b with
+    (a1,b1) then (a2,b2) = (a2 a1, a2 b1 + b2); fold the maps in chunks of
+    several sizes (inner folds first, then across chunks) and compare."""
+    c = small_case(seed=seed, with_z=False, with_h0=True)
+    _, hl = run(orc, c)
+    x = c["delta"].astype(np.float64) + c["delta_bias"].astype(np.float64)[None, :, None]
+    dt = softplus_ref(x)
+    a = np.exp(dt[:, :, None, :] * c["A"].astype(np.float64)[None, :, :, None])   # (b,d,n,t)
+    b = dt[:, :, None, :] * c["B"].astype(np.float64)[:, None] * c["u"].astype(np.float64)[:, :, None]
+    L = a.shape[-1]
+    err = 0.0
+    for sizes in chunkings:
+        bounds, pos, k = [], 0, 0
+        while pos < L:
+            s = sizes[k % len(sizes)]
+            bounds.append((pos, min(L, pos + s)))
+            pos += s
+            k += 1
+        pairs = []
+        for lo, hi in bounds:
+            pa, pb = np.ones_like(a[..., 0]), np.zeros_like(b[..., 0])
+            for t in range(lo, hi):
+                pa, pb = a[..., t] * pa, a[..., t] * pb + b[..., t]
+            pairs.append((pa, pb))
+        # combine chunk summaries pairwise as a balanced tree
+        while len(pairs) > 1:
+            nxt = []
+            for i in range(0, len(pairs) - 1, 2):
+                (a1, b1), (a2, b2) = pairs[i], pairs[i + 1]
+                nxt.append((a2 * a1, a2 * b1 + b2))
+            if len(pairs) % 2:
+                nxt.append(pairs[-1])
+            pairs = nxt
+        PA, PB = pairs[0]
+        err = max(err, rel_err(PA * c["h0"] + PB, hl))
+    return err
+
+
+def pin_decode_chain(orc, seed=9, k=12):
+    """k chained single-token updates equal one scan of length k from the same h0."""
+    c = small_case(seed=seed, with_h0=True, L=k)
+    y, hl = run(orc, c)
+    state = np.ascontiguousarray(c["h0"].astype(np.float64))
+    ys = []
+    for t in range(k):
+        ys.append(orc.state_update(state, c["u"][..., t].copy(), c["delta"][..., t].copy(),
+                                   c["A"], c["B"][..., t].copy(), c["C"][..., t].copy(), D=c["D"],
+                                   dt_bias=c["delta_bias"], z=c["z"][..., t].copy()))
+    return max(rel_err(np.stack(ys, axis=-1), y), rel_err(state, hl))
+
+
+def pin_no_softplus(orc, seed=10):
+    """delta_softplus off: dt = delta + bias is used as given (kept positive here)."""
+    c = small_case(seed=seed)
+    c["delta"] = np.abs(c["delta"]) * 0.3
+    c["delta_bias"] = np.abs(c["delta_bias"]) * 0.1
+    c["delta_softplus"] = False
+    y, hl = run(orc, c)
+    y_ref, H = materialised_scan(c)
+    return max(rel_err(y, y_ref), rel_err(hl, H[..., -1]))
+
+
+ALL_PINS = {
+    "materialised": pin_materialised,
+    "materialised_h0_noz": lambda o: pin_materialised(o, seed=11, with_h0=True, with_z=False),
+    "lti_convolution": pin_lti_convolution,
+    "single_step": pin_single_step,
+    "zero_input": pin_zero_input,
+    "gated_rnn": pin_gated_rnn,
+    "geometric_decay": pin_geometric_decay,
+    "small_delta": pin_small_delta,
+    "chunk_split": pin_chunk_split,
+    "associative_scan": pin_associative_scan,
+    "decode_chain": pin_decode_chain,
+    "no_softplus": pin_no_softplus,
+}
+
+# every pin must come in under this (fp64 everywhere)
+PIN_TOL = {"small_delta": 1e-9}
+DEFAULT_TOL = 1e-11

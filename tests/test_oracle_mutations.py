@@ -1,0 +1,71 @@
+"""Plant plausible mistakes in a copy of the oracle and check the pins catch each.
+
+Every mutant is a text edit of oracle/ss_oracle.c compiled into a temporary
+library on the CPU; the real oracle is untouched. A mutant that survives every
+pin would mean the pins do not constrain that part of the oracle.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "ss_oracle.c")
+
+MUTANTS = {
+    "exp_sign": ("exp(dt * a)", "exp(-dt * a)"),
+    "drop_dt_in_input": ("dt * Bv * uv", "Bv * uv"),
+    "B_transposed": ("rd(j->B, bcrow + (long long)n * L + l", "rd(j->B, bcrow + l * N + n"),
+    "C_reads_B": ("rd(j->C, bcrow", "rd(j->B, bcrow"),
+    "drop_D_skip": ("yv += Dd * uv;", ";"),
+    "gate_before_skip": ("yv += Dd * uv;\n            if (j->z) yv *= ss_oracle_silu(rd(j->z, urow + l, j->dtype));",
+                         "if (j->z) yv *= ss_oracle_silu(rd(j->z, urow + l, j->dtype));\n            yv += Dd * uv;"),
+    "softplus_branch": ("log1p(exp(x));", "log(exp(x));"),
+    "softplus_sign": ("x + log1p(exp(-x))", "x + log1p(exp(x))"),
+    "ignore_h0": ("h[n] = j->h0 ? j->h0[r * N + n] : 0.0;", "h[n] = 0.0;"),
+    "output_before_update": (
+        "h[n] = exp(dt * a) * h[n] + dt * Bv * uv;\n                yv += Cv * h[n];",
+        "yv += Cv * h[n];\n                h[n] = exp(dt * a) * h[n] + dt * Bv * uv;"),
+    "sigmoid_not_silu": ("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
+    "bias_by_batch": ("j->bias[d]", "j->bias[b % j->dim]"),
+    "A_transposed": ("j->A[(long long)d * N + n]", "j->A[(long long)n * j->dim + d]"),
+    "u_lagged": ("const double uv = rd(j->u, urow + l, j->dtype);",
+                 "const double uv = rd(j->u, urow + (l > 0 ? l - 1 : 0), j->dtype);"),
+    "z_ignored": ("if (j->z) yv *=", "if (0) yv *="),
+    "D_by_n": ("(double)j->D[d]", "(double)j->D[0]"),
+}
+
+
+def _build(name, tmp_path):
+    text = open(SRC).read()
+    old, new = MUTANTS[name]
+    assert text.count(old) == 1, "mutation anchor not found once: %s" % name
+    src = tmp_path / ("m_%s.c" % name)
+    src.write_text(text.replace(old, new))
+    lib = tmp_path / ("m_%s.so" % name)
+    subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-o", str(lib), str(src), "-lm",
+                           "-lpthread"])
+    return str(lib)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path, monkeypatch):
+    oracle._load()
+    lib = ctypes.CDLL(_build(name, tmp_path))
+    real = oracle._lib
+    for fn in ("ss_oracle_scan", "ss_oracle_state_update", "ss_oracle_softplus", "ss_oracle_silu"):
+        f = getattr(lib, fn)
+        f.argtypes = getattr(real, fn).argtypes
+        f.restype = getattr(real, fn).restype
+    monkeypatch.setattr(oracle, "_lib", lib)
+    failed = []
+    for pname, pin in pins.ALL_PINS.items():
+        with np.errstate(all="ignore"):
+            err = pin(oracle)
+        if not (err <= pins.PIN_TOL.get(pname, pins.DEFAULT_TOL)):
+            failed.append(pname)
+    assert failed, "mutant %s passed every pin" % name
