@@ -1,0 +1,466 @@
+"""Benchmark: selective scan (S6) forward on one B300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one ss_scan_fwd over the Mamba-2.8B block shape (batch 8, d_inner
+5120, d_state 16, L 2048; bf16 u/delta/z/B/C, fp32 state and output, z gate
+and D skip on, final state written). Inputs are seeded synthetic draws
+(workloads.CONFIGS["mamba2p8b"]); 843 MB move per step, more than the 126 MB
+L2, so no flush is needed between steps.
+
+Prints one JSON line. `value` is elements/s (batch * d_inner * L per second)
+with inputs resident in HBM, summed over ranks; `e2e` repeats the metric with
+host buffers (pinned H2D of the inputs and D2H of y and h_last inside the
+timed region); `roofline` compares the kernel with the HBM and ALU floors;
+`cpu_baseline` times the fp64 oracle on a bounded sample on the host cores.
+Under torchrun every rank runs its own replica (rows are independent: no
+collective on the data path); only the timing is reduced (max over ranks).
+
+--impl reference times the fp64 CPU oracle itself (the only reference this
+project has) on the same metric, as a bounded row sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+CONFIG = "mamba2p8b"
+MAX_SM_MHZ = 2032.0        # B300 maximum SM clock
+FALLBACK_HBM_GBS = 6400.0  # used only when MEASURED_PEAKS.json is absent
+FP32_LANES_PER_SM = 128    # FMA-pipe lanes per SM per clock
+METRIC = "selective-scan elements/s (B*D*L) and HBM GB/s as % of roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=CONFIG)
+    ap.add_argument("--variant", default="auto", choices=["auto", "rows", "chunked", "simple"])
+    ap.add_argument("--tpr", type=int, default=0, help="threads per row (rows variant)")
+    ap.add_argument("--segments", type=int, default=0)
+    ap.add_argument("--skip-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--skip-e2e", action="store_true", help="skip the host-buffer e2e leg")
+    ap.add_argument("--skip-probe", action="store_true", help="skip the ALU-rate probes")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def step_bytes(cfg, out_bytes=4):
+    """Algorithmic bytes of one scan: read u, delta, z, B, C once; write y and
+    h_last; read A, D, delta_bias."""
+    esz = 2 if cfg.in_dtype == "bf16" else 4
+    bdl = cfg.batch * cfg.dim * cfg.seqlen
+    bnl = cfg.batch * cfg.dstate * cfg.seqlen
+    return (3 * bdl * esz + 2 * bnl * esz + bdl * out_bytes
+            + cfg.batch * cfg.dim * cfg.dstate * 4 + cfg.dim * cfg.dstate * 4 + 2 * cfg.dim * 4)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return float(d["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def time_oracle(cfg, seconds, threads):
+    """Time the fp64 oracle on as many rows of cfg as fit in about `seconds`.
+    Returns (elements/s, rows, L, elapsed)."""
+    import oracle
+    oracle.build()
+
+    def run(rows):
+        inp = workloads.scan_inputs(cfg, rows=rows)
+        t0 = time.perf_counter()
+        oracle.scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], D=inp["D"],
+                        delta_bias=inp["delta_bias"], z=inp["z"], rows=rows, dim=cfg.dim,
+                        threads=threads)
+        return time.perf_counter() - t0
+
+    g = np.random.default_rng(0)
+    calib = max(threads, 8)
+    rows = np.sort(g.choice(cfg.rows, size=min(calib, cfg.rows), replace=False))
+    t = run(rows)
+    per_row = t / len(rows)
+    n = int(min(cfg.rows, max(len(rows), seconds / max(per_row, 1e-9) * 1.0)))
+    n = max(threads, (n // threads) * threads) if n >= threads else n
+    rows = np.sort(g.choice(cfg.rows, size=min(n, cfg.rows), replace=False))
+    t = run(rows)
+    return len(rows) * cfg.seqlen / t, len(rows), cfg.seqlen, t
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self, t0, t1):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons, n = [], None, set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            if not (t0 - 0.15 <= ts <= t1 + 0.15):
+                continue
+            n += 1
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ---------------------------------------------------------------- ALU probe
+
+def probe_alu(device):
+    import ctypes
+    path = os.path.join(ROOT, "selective_state_space_136_b300", "libss_probe.so")
+    lib = ctypes.CDLL(path)
+    lib.ss_probe_alu.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                 ctypes.POINTER(ctypes.c_double)]
+    out = {}
+    for which, name in ((0, "ex2"), (1, "ffma"), (2, "ffma2")):
+        r, g = ctypes.c_double(), ctypes.c_double()
+        rc = lib.ss_probe_alu(which, device, ctypes.byref(r), ctypes.byref(g))
+        out[name] = {"ops_per_s": r.value, "sm_ghz": g.value, "rc": rc}
+    return out
+
+
+# ---------------------------------------------------------------- traffic from committed ncu summary
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("ss_rows.cu", "ss_common.cuh"):
+        h.update(open(os.path.join(ROOT, "selective_state_space_136_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(cfg_name):
+    """dram bytes per launch recorded in profiles/, if taken on this exact source."""
+    p = os.path.join(ROOT, "profiles", "ncu_scan_rows_%s.md" % cfg_name)
+    if not os.path.exists(p):
+        return None
+    sha, traffic = None, None
+    for line in open(p):
+        if line.startswith("source_sha:"):
+            sha = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            try:
+                traffic = float(line.split(":", 1)[1].strip())
+            except ValueError:
+                traffic = None
+    return traffic if sha == kernel_source_sha() else None
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import torch
+    import selective_state_space_136_b300 as ss
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    cfg = workloads.CONFIGS[args.config]
+    inp = workloads.scan_inputs(cfg)
+    shp = (cfg.batch, cfg.dim, cfg.seqlen)
+
+    def host_tensor(a, shape):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).reshape(shape)
+        return torch.from_numpy(a).reshape(shape)
+
+    host = {k: host_tensor(inp[k], shp) for k in ("u", "delta", "z")}
+    host["B"] = host_tensor(inp["B"], inp["B"].shape)
+    host["C"] = host_tensor(inp["C"], inp["C"].shape)
+    params = {k: torch.from_numpy(inp[k]).to(dev) for k in ("A", "D", "delta_bias")}
+    d = {k: v.to(dev) for k, v in host.items()}
+    y = torch.empty(shp, dtype=torch.float32, device=dev)
+    h_last = torch.empty((cfg.batch, cfg.dim, cfg.dstate), dtype=torch.float32, device=dev)
+
+    ctx = ss.Context(local)
+    ctx.set_option(ss.SS_OPT_VARIANT, {"auto": 0, "rows": 1, "chunked": 2, "simple": 3}[args.variant])
+    ctx.set_option(ss.SS_OPT_THREADS_PER_ROW, args.tpr)
+    ctx.set_option(ss.SS_OPT_SEGMENTS, args.segments)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(t):
+        ss.ss_scan_fwd(t["u"], t["delta"], params["A"], t["B"], t["C"], D=params["D"],
+                       delta_bias=params["delta_bias"], z=t["z"], y=y, h_last=h_last, ctx=ctx,
+                       stream=stream)
+
+    probes = None if args.skip_probe else probe_alu(local)
+
+    for _ in range(max(args.warmup, 0)):
+        step(d)
+    torch.cuda.synchronize(dev)
+    if ctx.device_error() != ss.SS_OK:
+        raise RuntimeError("device error during warm-up")
+    variant, launches_per_step = ctx.last_launch()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    t_wall0 = time.perf_counter()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step(d)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.perf_counter()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop(t_wall0, t_wall1)
+    per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    if ctx.device_error() != ss.SS_OK:
+        raise RuntimeError("device error in the timed region")
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    elements = cfg.elements
+    value = world * elements * args.steps / (total_ms * 1e-3)
+    ms_per_step = total_ms / args.steps
+    avg_launch_s = float(np.mean(per_launch_ms)) * 1e-3 / max(launches_per_step, 1)
+
+    # ---- end to end: pinned host inputs in, y and h_last back to host, every step
+    e2e = None
+    if not args.skip_e2e:
+        pinned = {k: v.pin_memory() for k, v in host.items()}
+        y_host = torch.empty(shp, dtype=torch.float32).pin_memory()
+        h_host = torch.empty((cfg.batch, cfg.dim, cfg.dstate), dtype=torch.float32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+        d2h = y_host.numel() * 4 + h_host.numel() * 4
+        dd = {k: torch.empty_like(v) for k, v in d.items()}
+
+        def e2e_step():
+            for k in dd:
+                dd[k].copy_(pinned[k], non_blocking=True)
+            step(dd)
+            y_host.copy_(y, non_blocking=True)
+            h_host.copy_(h_last, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        k_e2e = max(1, min(args.steps, 5))
+        if pg:
+            pg.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(b)
+        if pg:
+            t = torch.tensor([e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * elements * k_e2e / (e_ms * 1e-3), "unit": "elements/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k_e2e}
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    # ---- roofline of the (single) scan kernel
+    hbm_peak, hbm_src = measured_peaks()
+    nbytes = step_bytes(cfg)
+    gbs = nbytes / avg_launch_s / 1e9
+    bdln = elements * cfg.dstate
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    terms = {"hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "peak_source": hbm_src,
+                     "floor_us": nbytes / (hbm_peak * 1e9) * 1e6}}
+    fp32_peak = sms * FP32_LANES_PER_SM * MAX_SM_MHZ * 1e6 / 1e12     # Tops/s
+    fp32_ops = 4.0 * bdln
+    terms["fp32"] = {"achieved": fp32_ops / avg_launch_s / 1e12, "peak": fp32_peak,
+                     "unit": "Tops/s", "floor_us": fp32_ops / (fp32_peak * 1e12) * 1e6,
+                     "note": "4 FMA-pipe lane ops per state element (dt*A, dt*u*B, state FMA, "
+                             "output FMA) against %d lanes/SM at %.0f MHz" % (FP32_LANES_PER_SM,
+                                                                             MAX_SM_MHZ)}
+    if probes and probes["ex2"]["rc"] == 0 and probes["ex2"]["sm_ghz"] > 0:
+        per_clk = probes["ex2"]["ops_per_s"] / (sms * probes["ex2"]["sm_ghz"] * 1e9)
+        per_clk_arch = float(2 ** round(np.log2(max(per_clk, 1e-9))))
+        ex2_peak = sms * per_clk_arch * MAX_SM_MHZ * 1e6 / 1e9            # Gex2/s
+        terms["ex2"] = {"achieved": bdln / avg_launch_s / 1e9, "peak": ex2_peak,
+                        "unit": "Gex2/s", "floor_us": bdln / (ex2_peak * 1e9) * 1e6,
+                        "ex2_per_clk_per_sm_measured": per_clk,
+                        "ex2_per_clk_per_sm_used": per_clk_arch}
+    for t in terms.values():
+        t["frac"] = t["achieved"] / t["peak"]
+    dominant = max(terms, key=lambda k: terms[k]["floor_us"])
+    dt = terms[dominant]
+    roofline = {"bound": "hbm" if dominant == "hbm" else "alu", "term": dominant,
+                "achieved": dt["achieved"], "peak": dt["peak"], "unit": dt["unit"],
+                "frac": dt["frac"], "traffic": committed_traffic(args.config),
+                "algorithmic_bytes_per_launch": nbytes,
+                "kernel_us": avg_launch_s * 1e6,
+                "floor_us": max(t["floor_us"] for t in terms.values()),
+                "frac_of_floor": max(t["floor_us"] for t in terms.values()) / (avg_launch_s * 1e6),
+                "terms": terms, "peak_clock_mhz": MAX_SM_MHZ}
+
+    cpu = None
+    if not args.skip_cpu:
+        cores = cpu_cores()
+        v, nrows, L, el = time_oracle(cfg, args.cpu_seconds, cores)
+        cpu = {"value": v, "unit": "elements/s", "cores": cores, "kind": "oracle",
+               "sample": "%d of %d rows (b,d) x full L=%d of %s, fp64 C oracle, %.1f s"
+                         % (nrows, cfg.rows, L, args.config, el)}
+
+    names = {0: "auto", 1: "rows", 2: "chunked", 3: "simple"}
+    out = {
+        "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded normal draws; A=-(n+1); dt bias log-uniform [1e-3,1e-1])",
+        "config": {"workload": "%s: batch %d, d_inner %d, d_state %d, L %d, %s u/delta/z/B/C, "
+                               "fp32 state/y, z gate + D skip, h_last out"
+                               % (cfg.name, cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen,
+                                  cfg.in_dtype),
+                   "batch": cfg.batch, "d_inner": cfg.dim, "d_state": cfg.dstate,
+                   "seq_len": cfg.seqlen, "in_dtype": cfg.in_dtype, "out_dtype": "f32",
+                   "variant": names.get(variant, str(variant)),
+                   "l2": "no flush: %.0f MB of inputs+outputs per step > 126 MB L2" % (nbytes / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "gbs": gbs,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": int(args.steps * launches_per_step),
+        "alu_probe": probes,
+        "impl": "ours",
+    }
+    print(json.dumps(out), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    cfg = workloads.CONFIGS[args.config]
+    cores = cpu_cores()
+    per_step = max(1.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        time_oracle(cfg, per_step / 4, cores)
+    vals, rows_done, secs = [], 0, 0.0
+    for _ in range(args.steps):
+        v, nrows, L, el = time_oracle(cfg, per_step, cores)
+        vals.append(v)
+        rows_done += nrows
+        secs += el
+    value = float(np.mean(vals))
+    sample = ("per step %d-ish of %d rows x full L=%d of %s, fp64 C oracle on %d host threads"
+              % (rows_done // max(1, args.steps), cfg.rows, cfg.seqlen, args.config, cores))
+    out = {"metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": cfg.elements / value * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": cfg.name, "batch": cfg.batch, "d_inner": cfg.dim,
+                      "d_state": cfg.dstate, "seq_len": cfg.seqlen},
+           "impl": "reference",
+           "cpu_baseline": {"value": value, "unit": "elements/s", "cores": cores,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0},
+           "gpu_launches": 0}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

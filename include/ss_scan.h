@@ -1,0 +1,200 @@
+/*
+ * ss_scan: selective scan (S6) forward pass and single-token state update for
+ * NVIDIA B300 (sm_103a).
+ *
+ * C ABI. Plain pointers and sizes; no CUDA or framework types beyond the
+ * opaque stream handle, which is a cudaStream_t (pass NULL for the legacy
+ * default stream).
+ *
+ * The operation, by page title and section:
+ *  - "Mamba: Linear-Time Sequence Modeling with Selective State Spaces",
+ *    section "Method": zero-order-hold discretisation A_bar = exp(Delta A) and
+ *    the linear recurrence h_t = A_bar h_{t-1} + B_bar x_t, y_t = C h_t.
+ *  - same page, section "The Selection Mechanism (S6)": B_t, C_t (width N,
+ *    shared over channels) and Delta_t = softplus(parameter + projection)
+ *    depend on the input token.
+ *  - soft186.com, "Mamba选择性状态空间机制", section "动态参数化的状态空间":
+ *    dt = softplus(projection + delta_bias), dA = exp(dt * A), the state is
+ *    multiplied by dA and receives the input times dt * B.
+ *  - same Mamba page, sections "Hardware-aware state expansion" and
+ *    "Questions": the expanded state (batch, L, dim, N) never goes to device
+ *    memory; only the contracted output (batch, dim, L) is written; decoding
+ *    keeps a fixed dim x N state per sequence and advances it one token at a
+ *    time.
+ *
+ * Per row (b, d) and time step l the library computes
+ *     dt  = softplus(delta[b,d,l] + delta_bias[d])    (or the sum itself)
+ *     h_n = exp(dt * A[d,n]) * h_n + dt * B[b,n,l] * u[b,d,l]     n < N
+ *     y   = (sum_n C[b,n,l] * h_n + D[d] * u[b,d,l]) * silu(z[b,d,l])
+ * with the state h held in fp32 on chip and h_N after the last step
+ * optionally written out.
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, C-contiguous,
+ *    16-byte aligned. The library never frees or retains them.
+ *  - Calls are asynchronous and stream-ordered on the given stream; they do
+ *    not synchronise. Argument errors are detected on the host before any
+ *    launch and returned immediately (nothing is enqueued).
+ *  - Errors found on the device (a bounded wait that ran out) are recorded in
+ *    a per-context error word; read it with ss_get_device_error.
+ *  - A context must not be used from two host threads at once. Two streams
+ *    may share a context only for ss_state_update calls; a chunked
+ *    ss_scan_fwd uses context scratch, so give each concurrent stream its own
+ *    context.
+ */
+#ifndef SS_SCAN_H
+#define SS_SCAN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *ss_stream_t; /* == cudaStream_t */
+
+typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
+
+typedef enum {
+    SS_OK = 0,
+    SS_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or aliasing */
+    SS_ERR_UNSUPPORTED = 2,  /* valid but not built (e.g. dstate not in {1,2,4,8,16}) */
+    SS_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+    SS_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up */
+    SS_ERR_DEVICE = 5        /* other device-detected error */
+} ss_status;
+
+typedef struct ss_ctx ss_ctx;
+
+/*
+ * Create a context bound to CUDA device `device`. It queries the device
+ * (SM count, shared memory) and owns a small device buffer holding the error
+ * word; chunk-carry scratch is allocated on first need and kept.
+ * *out receives the context. Returns SS_OK, SS_ERR_INVALID_ARG (out NULL) or
+ * SS_ERR_CUDA.
+ */
+int ss_create(ss_ctx **out, int device);
+
+/* Free a context and its scratch. NULL is accepted. Synchronises the device. */
+int ss_destroy(ss_ctx *ctx);
+
+/*
+ * Selective scan forward.
+ *   batch, dim, dstate, seqlen : Bt, D (= d_inner), N, L. dim >= 1, batch >= 1,
+ *                                dstate in {1,2,4,8,16}, seqlen >= 0.
+ *   in_dtype   : dtype of u, delta, z, B, C (SS_F32 or SS_BF16).
+ *   out_dtype  : dtype of y (SS_F32 or SS_BF16; bf16 rounds to nearest even).
+ *   u, delta, z: (batch, dim, seqlen). z may be NULL: no gate.
+ *   A          : (dim, dstate) fp32, real; entries are expected to be negative
+ *                (not checked).
+ *   B, C       : (batch, dstate, seqlen), input-dependent, shared by all d.
+ *   D, delta_bias : (dim) fp32; either may be NULL (treated as zero).
+ *   delta_softplus: nonzero -> dt = softplus(delta + bias); zero -> the sum.
+ *   h0         : (batch, dim, dstate) fp32 initial state, or NULL for zero.
+ *   y          : (batch, dim, seqlen) output. Must not overlap any input.
+ *   h_last     : (batch, dim, dstate) fp32 final state, or NULL. May equal h0
+ *                (read before written, per row).
+ * Returns SS_OK or an error from ss_status. seqlen == 0 writes h_last = h0
+ * (or zeros) and nothing else.
+ */
+typedef struct {
+    int batch, dim, dstate;
+    long long seqlen;
+    int in_dtype, out_dtype;
+    const void *u, *delta, *z;
+    const float *A;
+    const void *B, *C;
+    const float *D, *delta_bias;
+    int delta_softplus;
+    const float *h0;
+    void *y;
+    float *h_last;
+} ss_scan_args;
+
+int ss_scan_fwd(ss_ctx *ctx, const ss_scan_args *args, ss_stream_t stream);
+
+/*
+ * Single-token selective state update (decoding).
+ *   state  : (batch, dim, dstate) fp32, read and overwritten in place with the
+ *            state after this token.
+ *   x, dt, z : (batch, dim) in in_dtype; z may be NULL.
+ *   A      : (dim, dstate) fp32;  B, C : (batch, dstate) in in_dtype.
+ *   D, dt_bias : (dim) fp32 or NULL.  dt_softplus as delta_softplus above.
+ *   y      : (batch, dim) in out_dtype; must not overlap the inputs or state.
+ * The arithmetic is that of ss_scan_fwd with seqlen = 1 and h0 = h_last = state.
+ */
+typedef struct {
+    int batch, dim, dstate;
+    int in_dtype, out_dtype;
+    float *state;
+    const void *x, *dt, *z;
+    const float *A;
+    const void *B, *C;
+    const float *D, *dt_bias;
+    int dt_softplus;
+    void *y;
+} ss_update_args;
+
+int ss_state_update(ss_ctx *ctx, const ss_update_args *args, ss_stream_t stream);
+
+/*
+ * Synchronise `stream`, then return and clear the context's device error
+ * word: SS_OK when no device-side check fired since the last read,
+ * SS_ERR_TIMEOUT when a bounded wait gave up, SS_ERR_CUDA if the sync failed.
+ */
+int ss_get_device_error(ss_ctx *ctx, ss_stream_t stream);
+
+/* Static text for a status code. */
+const char *ss_status_string(int status);
+
+/*
+ * Kernel selection for ss_scan_fwd (default SS_VARIANT_AUTO).
+ *   SS_VARIANT_ROWS    : one pass; each row's time axis is walked in order by
+ *                        a small group of threads, inputs staged by TMA.
+ *   SS_VARIANT_CHUNKED : the time axis is cut into segments scanned in
+ *                        parallel; per-segment (decay, state) pairs are
+ *                        combined by an associative scan and the segments are
+ *                        re-scanned from their carried-in state.
+ *   SS_VARIANT_SIMPLE  : one thread per row, plain loads; used for shapes the
+ *                        staged kernels cannot take (e.g. seqlen % 8 != 0).
+ * Options (ss_set_option):
+ *   SS_OPT_VARIANT          one of ss_variant.
+ *   SS_OPT_SEGMENTS         segment count of the chunked variant (0 = auto).
+ *   SS_OPT_THREADS_PER_ROW  threads sharing one row's states in the rows
+ *                           variant for dstate 16: 1, 2 or 4 (0 = auto).
+ *   SS_OPT_WAIT_LIMIT       polls before a device-side wait gives up and
+ *                           reports SS_ERR_TIMEOUT (default 2^22, roughly a
+ *                           second; 1 .. 2^30).
+ *   SS_OPT_TEST_DROP_TILE   test hook: the rows kernel never issues the loads
+ *                           of this tile index, so its wait runs out and the
+ *                           timeout path is exercised (-1 = off, the default).
+ * Returns SS_OK or SS_ERR_INVALID_ARG (unknown option or value out of range).
+ */
+typedef enum {
+    SS_VARIANT_AUTO = 0,
+    SS_VARIANT_ROWS = 1,
+    SS_VARIANT_CHUNKED = 2,
+    SS_VARIANT_SIMPLE = 3
+} ss_variant;
+
+typedef enum {
+    SS_OPT_VARIANT = 0,
+    SS_OPT_SEGMENTS = 1,
+    SS_OPT_THREADS_PER_ROW = 2,
+    SS_OPT_WAIT_LIMIT = 3,
+    SS_OPT_TEST_DROP_TILE = 4
+} ss_option;
+
+int ss_set_option(ss_ctx *ctx, int option, long long value);
+
+/*
+ * Describe the last ss_scan_fwd / ss_state_update enqueued on this context:
+ * *variant receives the ss_variant that ran, *launches the number of kernels
+ * it enqueued. Either pointer may be NULL.
+ */
+int ss_last_launch(const ss_ctx *ctx, int *variant, int *launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SS_SCAN_H */

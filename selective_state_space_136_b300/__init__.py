@@ -1,0 +1,249 @@
+"""Python binding of the ss_scan CUDA library (selective scan S6, sm_103a).
+
+Argument marshalling only: every step of the scan and of the decode update
+runs in the CUDA kernels of libss_scan.so, reached through its C ABI
+(include/ss_scan.h). PyTorch supplies device memory and the current stream.
+There is no CPU fallback: if the library is missing, every call raises.
+
+    from selective_state_space_136_b300 import ss_scan_fwd, ss_state_update
+    y, h_last = ss_scan_fwd(u, delta, A, B, C, D=D, delta_bias=bias, z=z)
+    y = ss_state_update(state, x, dt, A, B, C, D=D, dt_bias=bias, z=z)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.environ.get("SS_SCAN_LIB") or os.path.join(_HERE, "libss_scan.so")
+
+SS_F32, SS_BF16 = 0, 1
+SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_CUDA, SS_ERR_TIMEOUT, SS_ERR_DEVICE = range(6)
+SS_VARIANT_AUTO, SS_VARIANT_ROWS, SS_VARIANT_CHUNKED, SS_VARIANT_SIMPLE = range(4)
+(SS_OPT_VARIANT, SS_OPT_SEGMENTS, SS_OPT_THREADS_PER_ROW, SS_OPT_WAIT_LIMIT,
+ SS_OPT_TEST_DROP_TILE) = range(5)
+
+_vp = ctypes.c_void_p
+
+
+class ScanArgs(ctypes.Structure):
+    """Mirror of ss_scan_args."""
+    _fields_ = [("batch", ctypes.c_int), ("dim", ctypes.c_int), ("dstate", ctypes.c_int),
+                ("seqlen", ctypes.c_longlong), ("in_dtype", ctypes.c_int),
+                ("out_dtype", ctypes.c_int), ("u", _vp), ("delta", _vp), ("z", _vp),
+                ("A", _vp), ("B", _vp), ("C", _vp), ("D", _vp), ("delta_bias", _vp),
+                ("delta_softplus", ctypes.c_int), ("h0", _vp), ("y", _vp), ("h_last", _vp)]
+
+
+class UpdateArgs(ctypes.Structure):
+    """Mirror of ss_update_args."""
+    _fields_ = [("batch", ctypes.c_int), ("dim", ctypes.c_int), ("dstate", ctypes.c_int),
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("state", _vp),
+                ("x", _vp), ("dt", _vp), ("z", _vp), ("A", _vp), ("B", _vp), ("C", _vp),
+                ("D", _vp), ("dt_bias", _vp), ("dt_softplus", ctypes.c_int), ("y", _vp)]
+
+
+class SSError(RuntimeError):
+    def __init__(self, status, what):
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+        self.status = status
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def lib():
+    """The loaded libss_scan.so (raises if it has not been built)."""
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libss_scan.so is missing: build it with "
+                                   "`python -m selective_state_space_136_b300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            L.ss_create.argtypes = [ctypes.POINTER(_vp), ctypes.c_int]
+            L.ss_destroy.argtypes = [_vp]
+            L.ss_scan_fwd.argtypes = [_vp, ctypes.POINTER(ScanArgs), _vp]
+            L.ss_state_update.argtypes = [_vp, ctypes.POINTER(UpdateArgs), _vp]
+            L.ss_get_device_error.argtypes = [_vp, _vp]
+            L.ss_status_string.argtypes = [ctypes.c_int]
+            L.ss_status_string.restype = ctypes.c_char_p
+            L.ss_set_option.argtypes = [_vp, ctypes.c_int, ctypes.c_longlong]
+            L.ss_last_launch.argtypes = [_vp, ctypes.POINTER(ctypes.c_int),
+                                         ctypes.POINTER(ctypes.c_int)]
+            for f in ("ss_create", "ss_destroy", "ss_scan_fwd", "ss_state_update",
+                      "ss_get_device_error", "ss_set_option", "ss_last_launch"):
+                getattr(L, f).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().ss_status_string(int(status)).decode()
+
+
+def _check(rc, what):
+    if rc != SS_OK:
+        raise SSError(rc, what)
+
+
+class Context:
+    """Owns one ss_ctx (bound to one device)."""
+
+    def __init__(self, device: int = 0):
+        self._h = _vp()
+        _check(lib().ss_create(ctypes.byref(self._h), int(device)), "ss_create")
+        self.device = int(device)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def set_option(self, option: int, value: int):
+        _check(lib().ss_set_option(self._h, int(option), int(value)), "ss_set_option")
+
+    def device_error(self, stream=None) -> int:
+        return lib().ss_get_device_error(self._h, _stream_ptr(stream, self.device))
+
+    def last_launch(self):
+        v, n = ctypes.c_int(), ctypes.c_int()
+        _check(lib().ss_last_launch(self._h, ctypes.byref(v), ctypes.byref(n)), "ss_last_launch")
+        return v.value, n.value
+
+    def close(self):
+        if self._h:
+            lib().ss_destroy(self._h)
+            self._h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+_ctx_cache = {}
+
+
+def default_context(device: int) -> Context:
+    c = _ctx_cache.get(device)
+    if c is None:
+        c = _ctx_cache[device] = Context(device)
+    return c
+
+
+def _stream_ptr(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return _vp(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return SS_F32
+    if t.dtype == torch.bfloat16:
+        return SS_BF16
+    raise TypeError("expected float32 or bfloat16, got %s" % t.dtype)
+
+
+def _p(t):
+    return None if t is None else _vp(t.data_ptr())
+
+
+def _need(t, name, shape=None, dtype=None, device=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s has dtype %s, expected %s" % (name, t.dtype, dtype))
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+
+
+def ss_scan_fwd(u, delta, A, B, C, D=None, delta_bias=None, z=None, delta_softplus=True,
+                h0=None, y=None, h_last=None, out_dtype=None, return_last_state=True,
+                ctx: Context | None = None, stream=None):
+    """Selective scan forward on the GPU.
+
+    u, delta, z: (batch, dim, L), B, C: (batch, N, L), all float32 or all
+    bfloat16. A: (dim, N) float32; D, delta_bias: (dim,) float32 or None;
+    h0: (batch, dim, N) float32 or None. y (batch, dim, L) and h_last
+    (batch, dim, N) are allocated when not given; y defaults to float32.
+    Returns (y, h_last) (h_last None when return_last_state is False and no
+    buffer was given). Asynchronous on the current stream."""
+    import torch
+    _need(u, "u")
+    batch, dim, L = u.shape
+    N = B.shape[1]
+    dev = u.device
+    _need(delta, "delta", u.shape, u.dtype, dev)
+    if z is not None:
+        _need(z, "z", u.shape, u.dtype, dev)
+    _need(B, "B", (batch, N, L), u.dtype, dev)
+    _need(C, "C", (batch, N, L), u.dtype, dev)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    if D is not None:
+        _need(D, "D", (dim,), torch.float32, dev)
+    if delta_bias is not None:
+        _need(delta_bias, "delta_bias", (dim,), torch.float32, dev)
+    if h0 is not None:
+        _need(h0, "h0", (batch, dim, N), torch.float32, dev)
+    if y is None:
+        y = torch.empty((batch, dim, L), dtype=out_dtype or torch.float32, device=dev)
+    _need(y, "y", (batch, dim, L), None, dev)
+    if h_last is None and return_last_state:
+        h_last = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    if h_last is not None:
+        _need(h_last, "h_last", (batch, dim, N), torch.float32, dev)
+    a = ScanArgs(batch, dim, N, L, _dtype_code(u), _dtype_code(y), _p(u), _p(delta), _p(z),
+                 _p(A), _p(B), _p(C), _p(D), _p(delta_bias), int(bool(delta_softplus)), _p(h0),
+                 _p(y), _p(h_last))
+    ctx = ctx or default_context(dev.index if dev.index is not None else 0)
+    _check(lib().ss_scan_fwd(ctx.handle, ctypes.byref(a), _stream_ptr(stream, dev)),
+           "ss_scan_fwd")
+    return y, h_last
+
+
+def ss_state_update(state, x, dt, A, B, C, D=None, dt_bias=None, z=None, dt_softplus=True,
+                    y=None, out_dtype=None, ctx: Context | None = None, stream=None):
+    """One decode step on the GPU; `state` (batch, dim, N) float32 is updated
+    in place. x, dt, z: (batch, dim); B, C: (batch, N); A: (dim, N) float32.
+    Returns y (batch, dim), float32 unless out_dtype/y say otherwise."""
+    import torch
+    _need(state, "state", None, torch.float32)
+    batch, dim, N = state.shape
+    dev = state.device
+    _need(x, "x", (batch, dim), None, dev)
+    _need(dt, "dt", (batch, dim), x.dtype, dev)
+    if z is not None:
+        _need(z, "z", (batch, dim), x.dtype, dev)
+    _need(B, "B", (batch, N), x.dtype, dev)
+    _need(C, "C", (batch, N), x.dtype, dev)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    if D is not None:
+        _need(D, "D", (dim,), torch.float32, dev)
+    if dt_bias is not None:
+        _need(dt_bias, "dt_bias", (dim,), torch.float32, dev)
+    if y is None:
+        y = torch.empty((batch, dim), dtype=out_dtype or torch.float32, device=dev)
+    _need(y, "y", (batch, dim), None, dev)
+    a = UpdateArgs(batch, dim, N, _dtype_code(x), _dtype_code(y), _p(state), _p(x), _p(dt),
+                   _p(z), _p(A), _p(B), _p(C), _p(D), _p(dt_bias), int(bool(dt_softplus)), _p(y))
+    ctx = ctx or default_context(dev.index if dev.index is not None else 0)
+    _check(lib().ss_state_update(ctx.handle, ctypes.byref(a), _stream_ptr(stream, dev)),
+           "ss_state_update")
+    return y
+
+
+__all__ = ["ss_scan_fwd", "ss_state_update", "Context", "SSError", "lib", "status_string",
+           "ScanArgs", "UpdateArgs", "LIB_PATH"]

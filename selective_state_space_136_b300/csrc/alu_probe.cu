@@ -1,0 +1,120 @@
+// Throughput probes for the two compute units the selective scan leans on:
+// the MUFU base-2 exponential and the FP32 FMA pipe (scalar and packed
+// fp32x2). Measurement support for the benchmark's compute roofline; not part
+// of the scan library.
+//
+// Each thread runs 8 independent dependency chains so the unit, not latency,
+// limits the rate. The kernel also records SM cycles (clock64) against the
+// global nanosecond timer in one thread, which gives the SM clock the probe
+// actually ran at.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace {
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void ffma2(float &a0, float &a1, float b0, float b1, float c0,
+                                      float c1) {
+    asm volatile(
+        "{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\tmov.b64 rc, {%4, %5};\n\t"
+        "fma.rn.f32x2 ra, ra, rb, rc;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+template <int WHICH>
+__global__ void __launch_bounds__(256) probe_kernel(float *sink, int iters,
+                                                    unsigned long long *clk) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = 0.25f + 0.01f * i + 1e-6f * threadIdx.x;
+    uint64_t c0 = 0, t0 = 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) c0 = clock64(), t0 = gtimer();
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if constexpr (WHICH == 0) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a[i] = ex2(-a[i]);
+            } else if constexpr (WHICH == 1) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a[i] = fmaf(a[i], 0.9990234375f, 0.0009765625f);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; i += 2)
+                    ffma2(a[i], a[i + 1], 0.9990234375f, 0.9990234375f, 0.0009765625f,
+                          0.0009765625f);
+            }
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        clk[0] = clock64() - c0;
+        clk[1] = gtimer() - t0;
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += a[i];
+    if (s == 1234.5f) sink[threadIdx.x] = s;  // keeps the chains live
+}
+
+}  // namespace
+
+extern "C" {
+
+// which: 0 = MUFU ex2, 1 = FFMA, 2 = packed FFMA2 (counted as 2 FMA each).
+// Writes the sustained rate in operations per second and the SM clock in GHz
+// seen by the probe. Returns 0 on success, the CUDA error code otherwise.
+int ss_probe_alu(int which, int device, double *ops_per_s, double *sm_ghz) {
+    cudaError_t e = cudaSetDevice(device);
+    if (e != cudaSuccess) return (int)e;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    float *sink = nullptr;
+    unsigned long long *clk = nullptr;
+    cudaMalloc(&sink, 256 * sizeof(float));
+    cudaMalloc(&clk, 2 * sizeof(unsigned long long));
+    cudaStream_t st;
+    cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    cudaEvent_t a, b;
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+    const int blocks = sms * 8, threads = 256;
+    const int iters = which == 0 ? 2048 : 8192;
+    auto run = [&](int n) {
+        if (which == 0) probe_kernel<0><<<blocks, threads, 0, st>>>(sink, n, clk);
+        else if (which == 1) probe_kernel<1><<<blocks, threads, 0, st>>>(sink, n, clk);
+        else probe_kernel<2><<<blocks, threads, 0, st>>>(sink, n, clk);
+    };
+    run(iters / 8);  // warm-up
+    cudaEventRecord(a, st);
+    run(iters);
+    cudaEventRecord(b, st);
+    e = cudaEventSynchronize(b);
+    float ms = 0.f;
+    unsigned long long hc[2] = {0, 0};
+    if (e == cudaSuccess) {
+        cudaEventElapsedTime(&ms, a, b);
+        cudaMemcpy(hc, clk, sizeof(hc), cudaMemcpyDeviceToHost);
+        const double ops = (double)blocks * threads * iters * 32.0;  // 4 x 8 per iteration
+        if (ops_per_s) *ops_per_s = ops / (ms * 1e-3);
+        if (sm_ghz) *sm_ghz = hc[1] ? (double)hc[0] / (double)hc[1] : 0.0;
+    }
+    cudaEventDestroy(a);
+    cudaEventDestroy(b);
+    cudaStreamDestroy(st);
+    cudaFree(sink);
+    cudaFree(clk);
+    return (int)e;
+}
+
+}  // extern "C"

@@ -1,0 +1,253 @@
+// C ABI of the ss_scan library: context management, argument validation and
+// kernel selection. Every entry point validates on the host and returns an
+// ss_status; nothing is enqueued when validation fails.
+#include <stdint.h>
+#include <string.h>
+
+#include "ss_internal.h"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dtype(int t) { return t == SS_F32 || t == SS_BF16; }
+
+bool valid_dstate(int n) { return n == 1 || n == 2 || n == 4 || n == 8 || n == 16; }
+
+struct Span {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+Span span(const void *p, size_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Span{a, a + bytes};
+}
+bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+int set_device(const ss_ctx *ctx) {
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return SS_ERR_CUDA;
+    if (cur != ctx->device && cudaSetDevice(ctx->device) != cudaSuccess) return SS_ERR_CUDA;
+    return SS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ss_status_string(int status) {
+    switch (status) {
+        case SS_OK: return "ok";
+        case SS_ERR_INVALID_ARG: return "invalid argument";
+        case SS_ERR_UNSUPPORTED: return "unsupported configuration";
+        case SS_ERR_CUDA: return "CUDA runtime error";
+        case SS_ERR_TIMEOUT: return "device wait timed out";
+        case SS_ERR_DEVICE: return "device-side error";
+        default: return "unknown status";
+    }
+}
+
+int ss_create(ss_ctx **out, int device) {
+    if (!out) return SS_ERR_INVALID_ARG;
+    *out = nullptr;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
+        return SS_ERR_CUDA;
+    ss_ctx *c = new ss_ctx();
+    c->device = device;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (cudaSetDevice(device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, device) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&c->max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                               device) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void **>(&c->d_err), sizeof(int)) != cudaSuccess ||
+        cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) {
+        if (c->d_err) cudaFree(c->d_err);
+        delete c;
+        cudaSetDevice(prev);
+        return SS_ERR_CUDA;
+    }
+    cudaSetDevice(prev);
+    *out = c;
+    return SS_OK;
+}
+
+int ss_destroy(ss_ctx *ctx) {
+    if (!ctx) return SS_OK;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(ctx->device);
+    cudaDeviceSynchronize();
+    if (ctx->d_err) cudaFree(ctx->d_err);
+    if (ctx->scratch) cudaFree(ctx->scratch);
+    cudaSetDevice(prev);
+    delete ctx;
+    return SS_OK;
+}
+
+int ss_set_option(ss_ctx *ctx, int option, long long value) {
+    if (!ctx) return SS_ERR_INVALID_ARG;
+    switch (option) {
+        case SS_OPT_VARIANT:
+            if (value < SS_VARIANT_AUTO || value > SS_VARIANT_SIMPLE) return SS_ERR_INVALID_ARG;
+            ctx->variant = (int)value;
+            return SS_OK;
+        case SS_OPT_SEGMENTS:
+            if (value < 0 || value > 65535) return SS_ERR_INVALID_ARG;
+            ctx->segments = (int)value;
+            return SS_OK;
+        case SS_OPT_THREADS_PER_ROW:
+            if (value != 0 && value != 1 && value != 2 && value != 4) return SS_ERR_INVALID_ARG;
+            ctx->rows_tpr = (int)value;
+            return SS_OK;
+        case SS_OPT_WAIT_LIMIT:
+            if (value < 1 || value > (1LL << 30)) return SS_ERR_INVALID_ARG;
+            ctx->wait_limit = (uint32_t)value;
+            return SS_OK;
+        case SS_OPT_TEST_DROP_TILE:
+            if (value < -1 || value > (1LL << 30)) return SS_ERR_INVALID_ARG;
+            ctx->drop_tile = (int)value;
+            return SS_OK;
+        default: return SS_ERR_INVALID_ARG;
+    }
+}
+
+int ss_last_launch(const ss_ctx *ctx, int *variant, int *launches) {
+    if (!ctx) return SS_ERR_INVALID_ARG;
+    if (variant) *variant = ctx->last_variant;
+    if (launches) *launches = ctx->last_launches;
+    return SS_OK;
+}
+
+int ss_get_device_error(ss_ctx *ctx, ss_stream_t stream) {
+    if (!ctx) return SS_ERR_INVALID_ARG;
+    if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
+    int h = 0;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SS_ERR_CUDA;
+    if (cudaMemcpy(&h, ctx->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SS_ERR_CUDA;
+    if (h != 0 && cudaMemset(ctx->d_err, 0, sizeof(int)) != cudaSuccess) return SS_ERR_CUDA;
+    return h;
+}
+
+int ss_scan_fwd(ss_ctx *ctx, const ss_scan_args *a, ss_stream_t stream) {
+    if (!ctx || !a) return SS_ERR_INVALID_ARG;
+    if (a->batch < 1 || a->dim < 1 || a->seqlen < 0) return SS_ERR_INVALID_ARG;
+    if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return SS_ERR_INVALID_ARG;
+    if (!valid_dstate(a->dstate)) return SS_ERR_UNSUPPORTED;
+    if ((long long)a->batch * a->dim > (1LL << 40) || a->seqlen >= (1LL << 40))
+        return SS_ERR_INVALID_ARG;
+    const long long rows = (long long)a->batch * a->dim;
+    const size_t esz = a->in_dtype == SS_BF16 ? 2 : 4;
+    const size_t osz = a->out_dtype == SS_BF16 ? 2 : 4;
+    const size_t n_elem = (size_t)rows * (size_t)a->seqlen;
+    const size_t n_bc = (size_t)a->batch * a->dstate * (size_t)a->seqlen;
+    const size_t n_state = (size_t)rows * a->dstate;
+    if (!a->A) return SS_ERR_INVALID_ARG;
+    if (a->seqlen > 0 && (!a->u || !a->delta || !a->B || !a->C || !a->y))
+        return SS_ERR_INVALID_ARG;
+    const void *ptrs[] = {a->u, a->delta, a->z, a->A, a->B, a->C, a->D, a->delta_bias, a->h0,
+                          a->y, a->h_last};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return SS_ERR_INVALID_ARG;
+    // outputs must not overlap inputs (h_last == h0 is allowed: read then written per row)
+    if (a->seqlen > 0) {
+        const Span y = span(a->y, n_elem * osz);
+        const Span ins[] = {span(a->u, n_elem * esz), span(a->delta, n_elem * esz),
+                            span(a->z, a->z ? n_elem * esz : 0), span(a->B, n_bc * esz),
+                            span(a->C, n_bc * esz), span(a->A, (size_t)a->dim * a->dstate * 4),
+                            span(a->D, a->D ? (size_t)a->dim * 4 : 0),
+                            span(a->delta_bias, a->delta_bias ? (size_t)a->dim * 4 : 0),
+                            span(a->h0, a->h0 ? n_state * 4 : 0),
+                            span(a->h_last, a->h_last ? n_state * 4 : 0)};
+        for (const Span &s : ins)
+            if (overlaps(y, s)) return SS_ERR_INVALID_ARG;
+    }
+    if (a->h_last && a->h0 && a->h_last != a->h0 &&
+        overlaps(span(a->h_last, n_state * 4), span(a->h0, n_state * 4)))
+        return SS_ERR_INVALID_ARG;
+    if (a->h_last && a->seqlen > 0) {
+        const Span hl = span(a->h_last, n_state * 4);
+        const Span ins[] = {span(a->u, n_elem * esz), span(a->delta, n_elem * esz),
+                            span(a->z, a->z ? n_elem * esz : 0), span(a->B, n_bc * esz),
+                            span(a->C, n_bc * esz)};
+        for (const Span &s : ins)
+            if (overlaps(hl, s)) return SS_ERR_INVALID_ARG;
+    }
+    if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    ctx->last_launches = 0;
+
+    if (a->seqlen == 0) {
+        ctx->last_variant = SS_VARIANT_AUTO;
+        if (!a->h_last) return SS_OK;
+        cudaError_t e = a->h0 ? (a->h0 == a->h_last
+                                     ? cudaSuccess
+                                     : cudaMemcpyAsync(a->h_last, a->h0, n_state * 4,
+                                                       cudaMemcpyDeviceToDevice, st))
+                              : cudaMemsetAsync(a->h_last, 0, n_state * 4, st);
+        return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    }
+
+    ssh::ScanParams p{a->batch, a->dim, a->dstate, a->seqlen, a->in_dtype, a->out_dtype,
+                      a->u, a->delta, a->z, a->A, a->B, a->C, a->D, a->delta_bias,
+                      a->delta_softplus, a->h0, a->y, a->h_last, ctx->d_err, ctx->wait_limit,
+                      ctx->drop_tile};
+    int variant = ctx->variant;
+    const bool rows_ok = ssh::rows_supported(p) && ssh::seq_supported(p);
+    if (variant == SS_VARIANT_AUTO) variant = rows_ok ? SS_VARIANT_ROWS : SS_VARIANT_SIMPLE;
+    if (variant == SS_VARIANT_CHUNKED) return SS_ERR_UNSUPPORTED;
+    if (variant == SS_VARIANT_ROWS && !rows_ok) return SS_ERR_UNSUPPORTED;
+    int rc;
+    if (variant == SS_VARIANT_ROWS) {
+        const int tpr = ctx->rows_tpr ? ctx->rows_tpr : 1;
+        rc = tpr == 1 ? ssh::launch_seq(p, ctx->max_smem_optin, st)
+                      : ssh::launch_rows(p, tpr, ctx->max_smem_optin, st);
+    } else {
+        rc = ssh::launch_simple(p, st);
+    }
+    ctx->last_variant = variant;
+    ctx->last_launches = rc == SS_OK ? 1 : 0;
+    return rc;
+}
+
+int ss_state_update(ss_ctx *ctx, const ss_update_args *a, ss_stream_t stream) {
+    if (!ctx || !a) return SS_ERR_INVALID_ARG;
+    if (a->batch < 1 || a->dim < 1) return SS_ERR_INVALID_ARG;
+    if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return SS_ERR_INVALID_ARG;
+    if (!valid_dstate(a->dstate)) return SS_ERR_UNSUPPORTED;
+    if ((long long)a->batch * a->dim > (1LL << 40)) return SS_ERR_INVALID_ARG;
+    if (!a->state || !a->x || !a->dt || !a->A || !a->B || !a->C || !a->y)
+        return SS_ERR_INVALID_ARG;
+    const void *ptrs[] = {a->state, a->x, a->dt, a->z, a->A, a->B, a->C, a->D, a->dt_bias, a->y};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return SS_ERR_INVALID_ARG;
+    const size_t rows = (size_t)a->batch * a->dim;
+    const size_t esz = a->in_dtype == SS_BF16 ? 2 : 4;
+    const size_t osz = a->out_dtype == SS_BF16 ? 2 : 4;
+    const Span y = span(a->y, rows * osz);
+    const Span stt = span(a->state, rows * a->dstate * 4);
+    const Span ins[] = {stt, span(a->x, rows * esz), span(a->dt, rows * esz),
+                        span(a->z, a->z ? rows * esz : 0),
+                        span(a->A, (size_t)a->dim * a->dstate * 4),
+                        span(a->B, (size_t)a->batch * a->dstate * esz),
+                        span(a->C, (size_t)a->batch * a->dstate * esz),
+                        span(a->D, a->D ? (size_t)a->dim * 4 : 0),
+                        span(a->dt_bias, a->dt_bias ? (size_t)a->dim * 4 : 0)};
+    for (const Span &s : ins)
+        if (overlaps(y, s)) return SS_ERR_INVALID_ARG;
+    for (size_t i = 1; i < sizeof(ins) / sizeof(ins[0]); ++i)
+        if (overlaps(stt, ins[i])) return SS_ERR_INVALID_ARG;
+    if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
+    ssh::UpdateParams p{a->batch, a->dim, a->dstate, a->in_dtype, a->out_dtype, a->state,
+                        a->x, a->dt, a->z, a->A, a->B, a->C, a->D, a->dt_bias,
+                        a->dt_softplus, a->y};
+    const int rc = ssh::launch_update(p, reinterpret_cast<cudaStream_t>(stream));
+    ctx->last_variant = 0;
+    ctx->last_launches = rc == SS_OK ? 1 : 0;
+    return rc;
+}
+
+}  // extern "C"

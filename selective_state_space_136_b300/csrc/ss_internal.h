@@ -1,0 +1,69 @@
+// Host-side internals of the ss_scan library: the context and the launchers
+// each kernel file provides. Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ss_scan.h"
+
+struct ss_ctx {
+    int device = 0;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    int *d_err = nullptr;          // device error word (one int)
+    void *scratch = nullptr;       // chunk-carry scratch, grown on demand
+    size_t scratch_bytes = 0;
+    int variant = SS_VARIANT_AUTO;
+    int segments = 0;              // 0 = choose automatically
+    int rows_tpr = 0;              // threads per row for the rows kernel (0 = auto)
+    uint32_t wait_limit = 1u << 22;  // polls before a device wait gives up
+    int drop_tile = -1;            // test hook: a tile whose loads are never issued
+    int last_variant = 0;
+    int last_launches = 0;
+};
+
+namespace ssh {
+
+// Parameters common to the scan kernels (device pointers).
+struct ScanParams {
+    int batch, dim, dstate;
+    long long seqlen;
+    int in_dtype, out_dtype;
+    const void *u, *delta, *z;
+    const float *A;
+    const void *B, *C;
+    const float *D, *bias;
+    int softplus;
+    const float *h0;
+    void *y;
+    float *h_last;
+    int *err;
+    uint32_t wait_limit;
+    int drop_tile;
+};
+
+int launch_simple(const ScanParams &p, cudaStream_t st);
+// tpr: threads per row (1, 2 or 4 for dstate 16; ignored otherwise).
+int launch_rows(const ScanParams &p, int tpr, int max_smem_optin, cudaStream_t st);
+// True when the rows kernel can take these arguments (TMA constraints).
+bool rows_supported(const ScanParams &p);
+// One thread per row, all states in registers (the default for staged shapes).
+int launch_seq(const ScanParams &p, int max_smem_optin, cudaStream_t st);
+bool seq_supported(const ScanParams &p);
+
+struct UpdateParams {
+    int batch, dim, dstate;
+    int in_dtype, out_dtype;
+    float *state;
+    const void *x, *dt, *z;
+    const float *A;
+    const void *B, *C;
+    const float *D, *bias;
+    int softplus;
+    void *y;
+};
+int launch_update(const UpdateParams &p, cudaStream_t st);
+
+}  // namespace ssh

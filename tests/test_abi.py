@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads and exports what include/ss_scan.h declares
+(CPU only: no compute call is made without a GPU)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ss_scan.h")
+
+
+@pytest.fixture(scope="module")
+def built():
+    from selective_state_space_136_b300 import build
+    return build.build()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ss_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(built):
+    lib = ctypes.CDLL(built["libss_scan.so"])
+    names = _declared_functions()
+    assert {"ss_create", "ss_destroy", "ss_scan_fwd", "ss_state_update"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_struct_layout_matches_binding(built, tmp_path):
+    """ctypes mirrors of the argument structs have the C layout."""
+    import selective_state_space_136_b300 as ss
+    prog = tmp_path / "layout.c"
+    fields_scan = [f for f, _ in ss.ScanArgs._fields_]
+    fields_upd = [f for f, _ in ss.UpdateArgs._fields_]
+    body = ['#include <stdio.h>', '#include <stddef.h>', '#include "ss_scan.h"', "int main(void){",
+            'printf("%zu %zu\\n", sizeof(ss_scan_args), sizeof(ss_update_args));']
+    for f in fields_scan:
+        body.append('printf("S %s %%zu\\n", offsetof(ss_scan_args, %s));' % (f, f))
+    for f in fields_upd:
+        body.append('printf("U %s %%zu\\n", offsetof(ss_update_args, %s));' % (f, f))
+    body.append("return 0;}")
+    prog.write_text("\n".join(body))
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(prog)])
+    out = subprocess.check_output([str(exe)]).decode().split("\n")
+    s_size, u_size = map(int, out[0].split())
+    assert s_size == ctypes.sizeof(ss.ScanArgs)
+    assert u_size == ctypes.sizeof(ss.UpdateArgs)
+    for line in out[1:]:
+        if not line:
+            continue
+        kind, name, off = line.split()
+        cls = ss.ScanArgs if kind == "S" else ss.UpdateArgs
+        assert getattr(cls, name).offset == int(off), (kind, name)
+
+
+def test_host_validation_without_gpu(built):
+    import selective_state_space_136_b300 as ss
+    L = ss.lib()
+    assert L.ss_scan_fwd(None, None, None) == ss.SS_ERR_INVALID_ARG
+    assert L.ss_state_update(None, None, None) == ss.SS_ERR_INVALID_ARG
+    assert L.ss_set_option(None, 0, 0) == ss.SS_ERR_INVALID_ARG
+    assert L.ss_destroy(None) == ss.SS_OK
+    assert ss.status_string(ss.SS_ERR_TIMEOUT) == "device wait timed out"
+    assert ss.status_string(99) == "unknown status"
+
+
+def test_create_fails_cleanly_without_gpu(built):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    import selective_state_space_136_b300 as ss
+    h = ctypes.c_void_p()
+    assert ss.lib().ss_create(ctypes.byref(h), 0) == ss.SS_ERR_CUDA
+    assert not h.value
+
+
+def test_binding_refuses_cpu_tensors(built):
+    import torch
+    import selective_state_space_136_b300 as ss
+    x = torch.zeros(1, 4, 8)
+    with pytest.raises(ValueError):
+        ss.ss_scan_fwd(x, x, torch.zeros(4, 4), torch.zeros(1, 4, 8), torch.zeros(1, 4, 8))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import selective_state_space_136_b300 as ss
+    monkeypatch.setattr(ss, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(ss, "_lib", None)
+    with pytest.raises(RuntimeError):
+        ss.lib()
