@@ -158,9 +158,16 @@ const char *ss_status_string(int status);
  *                        staged kernels cannot take (e.g. seqlen % 8 != 0).
  * Options (ss_set_option):
  *   SS_OPT_VARIANT          one of ss_variant.
- *   SS_OPT_SEGMENTS         segment count of the chunked variant (0 = auto).
- *   SS_OPT_THREADS_PER_ROW  threads sharing one row's states in the rows
- *                           variant for dstate 16: 1, 2 or 4 (0 = auto).
+ *   SS_OPT_SEGMENTS         time segments per row block for the chained rows
+ *                           variant and the chunked variant (0 = auto).
+ *   SS_OPT_THREADS_PER_ROW  how the rows variant splits a row's states over
+ *                           threads: 1 = one thread per row (any dstate);
+ *                           2 = two threads share a pair of rows, time
+ *                           segments chained through the context scratch
+ *                           (dstate 16); 4 = four threads per row (dstate
+ *                           16); 0 = auto (2 for dstate 16, else 1).
+ *   SS_OPT_RESIDENT_WARPS   persistent warps per SM for the chained variant
+ *                           (default 8; 0 = as many as fit).
  *   SS_OPT_WAIT_LIMIT       polls before a device-side wait gives up and
  *                           reports SS_ERR_TIMEOUT (default 2^22, roughly a
  *                           second; 1 .. 2^30).
@@ -181,7 +188,8 @@ typedef enum {
     SS_OPT_SEGMENTS = 1,
     SS_OPT_THREADS_PER_ROW = 2,
     SS_OPT_WAIT_LIMIT = 3,
-    SS_OPT_TEST_DROP_TILE = 4
+    SS_OPT_TEST_DROP_TILE = 4,
+    SS_OPT_RESIDENT_WARPS = 5
 } ss_option;
 
 int ss_set_option(ss_ctx *ctx, int option, long long value);

@@ -23,6 +23,32 @@ Span span(const void *p, size_t bytes) {
 }
 bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
 
+// Grow the context scratch to hold the chained kernel's buffers; zero it when
+// (re)allocated (the flags must start below every epoch).
+int ensure_pair_scratch(ss_ctx *ctx, const ssh::ScanParams &p, ssh::PairWork *w) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t flags_b = up((size_t)ssh::pair_row_blocks(p) * 8);
+    const size_t carry_b = up(ssh::pair_carry_bytes(p));
+    const size_t bc_b = up(ssh::pair_bc_bytes(p));
+    const size_t need = 256 + flags_b + carry_b + bc_b;
+    if (need > ctx->scratch_bytes) {
+        if (ctx->scratch) {
+            if (cudaFree(ctx->scratch) != cudaSuccess) return SS_ERR_CUDA;
+            ctx->scratch = nullptr;
+            ctx->scratch_bytes = 0;
+        }
+        if (cudaMalloc(&ctx->scratch, need) != cudaSuccess) return SS_ERR_CUDA;
+        if (cudaMemset(ctx->scratch, 0, need) != cudaSuccess) return SS_ERR_CUDA;
+        ctx->scratch_bytes = need;
+    }
+    uint8_t *base = static_cast<uint8_t *>(ctx->scratch);
+    w->counter = reinterpret_cast<unsigned long long *>(base);
+    w->flags = reinterpret_cast<unsigned long long *>(base + 256);
+    w->carry = reinterpret_cast<float *>(base + 256 + flags_b);
+    w->bc = reinterpret_cast<float *>(base + 256 + flags_b + carry_b);
+    return SS_OK;
+}
+
 int set_device(const ss_ctx *ctx) {
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) return SS_ERR_CUDA;
@@ -100,6 +126,10 @@ int ss_set_option(ss_ctx *ctx, int option, long long value) {
         case SS_OPT_THREADS_PER_ROW:
             if (value != 0 && value != 1 && value != 2 && value != 4) return SS_ERR_INVALID_ARG;
             ctx->rows_tpr = (int)value;
+            return SS_OK;
+        case SS_OPT_RESIDENT_WARPS:
+            if (value < 0 || value > 64) return SS_ERR_INVALID_ARG;
+            ctx->warps_per_sm = (int)value;
             return SS_OK;
         case SS_OPT_WAIT_LIMIT:
             if (value < 1 || value > (1LL << 30)) return SS_ERR_INVALID_ARG;
@@ -200,16 +230,30 @@ int ss_scan_fwd(ss_ctx *ctx, const ss_scan_args *a, ss_stream_t stream) {
     if (variant == SS_VARIANT_AUTO) variant = rows_ok ? SS_VARIANT_ROWS : SS_VARIANT_SIMPLE;
     if (variant == SS_VARIANT_CHUNKED) return SS_ERR_UNSUPPORTED;
     if (variant == SS_VARIANT_ROWS && !rows_ok) return SS_ERR_UNSUPPORTED;
-    int rc;
+    int rc, launches = 1;
     if (variant == SS_VARIANT_ROWS) {
-        const int tpr = ctx->rows_tpr ? ctx->rows_tpr : 1;
-        rc = tpr == 1 ? ssh::launch_seq(p, ctx->max_smem_optin, st)
-                      : ssh::launch_rows(p, tpr, ctx->max_smem_optin, st);
+        int tpr = ctx->rows_tpr;
+        if (tpr == 0) tpr = ssh::pair_supported(p) ? 2 : 1;
+        if (tpr == 2) {
+            if (!ssh::pair_supported(p)) return SS_ERR_UNSUPPORTED;
+            ssh::PairWork w{};
+            if ((rc = ensure_pair_scratch(ctx, p, &w)) != SS_OK) return rc;
+            w.epoch = ++ctx->epoch;
+            w.sm_count = ctx->sm_count;
+            w.warps_per_sm = ctx->warps_per_sm;
+            w.n_seg = ctx->segments > 0 ? ctx->segments : 4;
+            rc = ssh::launch_pair(p, w, st);
+            launches = 2;
+        } else if (tpr == 1) {
+            rc = ssh::launch_seq(p, ctx->max_smem_optin, st);
+        } else {
+            rc = ssh::launch_rows(p, tpr, ctx->max_smem_optin, st);
+        }
     } else {
         rc = ssh::launch_simple(p, st);
     }
     ctx->last_variant = variant;
-    ctx->last_launches = rc == SS_OK ? 1 : 0;
+    ctx->last_launches = rc == SS_OK ? launches : 0;
     return rc;
 }
 

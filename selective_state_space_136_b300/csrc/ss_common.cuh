@@ -103,6 +103,58 @@ __device__ __forceinline__ f2 log1p_unit2(f2 w) {
     return fmul2(p, w);
 }
 
+// log1p(w) on [0, 1] for a single value: w * P6(w), P6 a degree-6 polynomial
+// fitted like the degree-7 one above (within 1.4e-6 relative of log1p(w)).
+__device__ __forceinline__ float log1p_unit(float w) {
+    float p = 1.414100733e-02f;
+    p = fmaf(p, w, -6.640174985e-02f);
+    p = fmaf(p, w, 1.492238194e-01f);
+    p = fmaf(p, w, -2.350385785e-01f);
+    p = fmaf(p, w, 3.310944736e-01f);
+    p = fmaf(p, w, -4.998696446e-01f);
+    p = fmaf(p, w, 9.999987483e-01f);
+    return p * w;
+}
+// softplus(x) = max(x, 0) + log1p(2^(-|x| log2 e)), branch-free (see softplus2).
+__device__ __forceinline__ float softplus1(float x) {
+    return fmaxf(x, 0.f) + log1p_unit(ex2(fabsf(x) * -kLog2e));
+}
+
+// Degree-6 variant of log1p_unit2 (within 1.4e-6 relative of log1p(w)).
+__device__ __forceinline__ f2 log1p_unit2_d6(f2 w) {
+    f2 p = mk2(1.414100733e-02f, 1.414100733e-02f);
+    p = ffma2(p, w, mk2(-6.640174985e-02f, -6.640174985e-02f));
+    p = ffma2(p, w, mk2(1.492238194e-01f, 1.492238194e-01f));
+    p = ffma2(p, w, mk2(-2.350385785e-01f, -2.350385785e-01f));
+    p = ffma2(p, w, mk2(3.310944736e-01f, 3.310944736e-01f));
+    p = ffma2(p, w, mk2(-4.998696446e-01f, -4.998696446e-01f));
+    p = ffma2(p, w, mk2(9.999987483e-01f, 9.999987483e-01f));
+    return fmul2(p, w);
+}
+__device__ __forceinline__ f2 softplus2_d6(f2 x) {
+    const f2 t = fmul2(mk2(fabsf(x.x), fabsf(x.y)), mk2(-kLog2e, -kLog2e));
+    const f2 w = mk2(ex2(t.x), ex2(t.y));
+    return fadd2(mk2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), log1p_unit2_d6(w));
+}
+
+// 256-bit (one 32-byte sector) per-thread global load / store (sm_100+).
+struct u8v {
+    uint32_t w[8];
+};
+__device__ __forceinline__ u8v ldg256(const void *p) {
+    u8v v;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]),
+                   "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void stg256(void *p, const float *f) {
+    asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(f[0]),
+                 "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7])
+                 : "memory");
+}
+
 // softplus on a pair: max(x, 0) + log1p(2^(-|x| log2 e)). No branch: for
 // x > ~17 the log1p term is below half an ulp of x; for x < -87 the
 // exponential flushes to zero and so does the result.

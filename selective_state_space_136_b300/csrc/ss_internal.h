@@ -18,6 +18,8 @@ struct ss_ctx {
     int variant = SS_VARIANT_AUTO;
     int segments = 0;              // 0 = choose automatically
     int rows_tpr = 0;              // threads per row for the rows kernel (0 = auto)
+    int warps_per_sm = 8;          // persistent warps per SM for the chained kernel
+    unsigned long long epoch = 0;  // calls that used the chained scratch
     uint32_t wait_limit = 1u << 22;  // polls before a device wait gives up
     int drop_tile = -1;            // test hook: a tile whose loads are never issued
     int last_variant = 0;
@@ -52,6 +54,23 @@ bool rows_supported(const ScanParams &p);
 // One thread per row, all states in registers (the default for staged shapes).
 int launch_seq(const ScanParams &p, int max_smem_optin, cudaStream_t st);
 bool seq_supported(const ScanParams &p);
+
+// Chained pair-row variant (dstate 16): scratch it needs and its launcher.
+struct PairWork {
+    float *bc;                       // packed fp32 B/C, pair_bc_bytes()
+    float *carry;                    // pair_carry_bytes()
+    unsigned long long *flags;       // one per row block, zeroed once at allocation
+    unsigned long long *counter;     // work counter, reset by the first kernel of a call
+    unsigned long long epoch;        // strictly increasing per call on this scratch
+    int n_seg;                       // time segments per row block
+    int warps_per_sm;                // persistent warps per SM (0 = as many as fit)
+    int sm_count;
+};
+size_t pair_bc_bytes(const ScanParams &p);
+size_t pair_carry_bytes(const ScanParams &p);
+int pair_row_blocks(const ScanParams &p);
+bool pair_supported(const ScanParams &p);
+int launch_pair(const ScanParams &p, const PairWork &w, cudaStream_t st);
 
 struct UpdateParams {
     int batch, dim, dstate;

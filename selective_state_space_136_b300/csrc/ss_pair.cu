@@ -1,0 +1,498 @@
+// Selective scan, chained pair-row variant (the default for dstate 16 when
+// there are many rows).
+//
+// What it computes is the selective recurrence of "Mamba: Linear-Time
+// Sequence Modeling with Selective State Spaces" (sections "Method" and "The
+// Selection Mechanism (S6)") with the dt * B input term of the soft186.com
+// article (section "动态参数化的状态空间"), fused as the Mamba page's section
+// "Hardware-aware state expansion" describes: inputs cross into on-chip
+// memory once, the 16 states of a row stay in registers, only y and the final
+// state are written.
+//
+// Two kernels per call:
+//  1. bc_pack: widens B and C ((batch, 16, L), bf16 or fp32) once into fp32
+//     rows [batch][L][B0..B15 C0..C15], the layout the scan reads, and resets
+//     the work counter of the call.
+//  2. scan_pair: persistent one-warp CTAs. A warp serves 32 rows of one batch
+//     as 16 row pairs; lane 2g+q owns row 2g+q for the per-row work (dt,
+//     dt*u, D skip, gate, loads and stores) and states [8q, 8q+8) of BOTH
+//     rows of its pair. Sharing each loaded B/C value between two rows halves
+//     the shared-memory bytes per state element; the partner row's dt and
+//     dt*u, and the partner's partial output, cross with one xor-shuffle each.
+//
+// Work is cut into units (time segment s, row block rb) taken from an atomic
+// counter in segment-major order, so the units of one row block are started
+// in time order. A unit starts from the state the previous segment of its
+// row block left in a global carry buffer (published with a release flag and
+// read after a bounded acquire wait). Segments only balance the load across
+// the machine: nothing is recomputed, and the exact order of the recurrence
+// along time is kept. A segment count of 1 gives plain static rows.
+//
+// Per tile of TL steps: the own row's u, delta, z arrive by cp.async into a
+// [tensor][chunk][lane] ring (conflict-free 128-bit reads); the fp32 B/C tile
+// arrives by one TMA box into an mbarrier-tracked ring. Steps past the end of
+// the sequence get dt = 0, an exact no-op on the state.
+#include "ss_common.cuh"
+#include "ss_internal.h"
+
+#include <cudaTypedefs.h>
+
+#ifndef SS_PAIR_TL
+#define SS_PAIR_TL 16
+#endif
+#ifndef SS_PAIR_S
+#define SS_PAIR_S 3
+#endif
+#ifndef SS_PAIR_MINB
+#define SS_PAIR_MINB 8
+#endif
+
+namespace {
+
+using namespace ssk;
+
+constexpr int kN = 16;  // states per row served by this variant
+
+template <typename Tin, int TL, int S>
+struct PairLayout {
+    static constexpr int ESZ = (int)sizeof(Tin);
+    static constexpr int NV = TL * ESZ / 32;           // 32-byte loads per row per tensor per tile
+    static constexpr int BC_BOX = TL * 2 * kN * 4;     // fp32 [TL][B16 C16]
+    static constexpr int OFF_BAR = S * BC_BOX;
+    static constexpr int TOTAL = OFF_BAR + S * 8 + 128;
+    static_assert(BC_BOX % 128 == 0, "TMA destinations 128-byte aligned");
+    static_assert(NV >= 1 && TL * ESZ % 32 == 0, "a tile row is whole 32-byte sectors");
+};
+
+// ---------------------------------------------------------------- B/C pack
+
+template <typename Tin>
+__global__ void __launch_bounds__(256) bc_pack_kernel(const Tin *__restrict__ B,
+                                                      const Tin *__restrict__ C, float *BC,
+                                                      long long L, int batch,
+                                                      unsigned long long *counter) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // (b, l)
+    if (i == 0 && counter) *counter = 0ull;
+    if (i >= (long long)batch * L) return;
+    const long long b = i / L, l = i % L;
+    const Tin *Bb = B + b * kN * L + l;
+    const Tin *Cb = C + b * kN * L + l;
+    float4 *dst = reinterpret_cast<float4 *>(BC + i * 2 * kN);
+#pragma unroll
+    for (int n = 0; n < kN; n += 4)
+        dst[n / 4] = make_float4(to_f32(Bb[n * L]), to_f32(Bb[(n + 1) * L]),
+                                 to_f32(Bb[(n + 2) * L]), to_f32(Bb[(n + 3) * L]));
+#pragma unroll
+    for (int n = 0; n < kN; n += 4)
+        dst[4 + n / 4] = make_float4(to_f32(Cb[n * L]), to_f32(Cb[(n + 1) * L]),
+                                     to_f32(Cb[(n + 2) * L]), to_f32(Cb[(n + 3) * L]));
+}
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ f2 pair_at(const uint32_t *w, int i, uint16_t) {
+    return mk2(bf16lo(w[i]), bf16hi(w[i]));
+}
+__device__ __forceinline__ f2 pair_at(const uint32_t *w, int i, float) {
+    return mk2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Store one tile of a row (32-byte aligned) as whole 32-byte sectors.
+template <int V>
+__device__ __forceinline__ void store_tile(float *dst, const float *v) {
+#pragma unroll
+    for (int j = 0; j < V / 8; ++j) stg256(dst + 8 * j, v + 8 * j);
+}
+template <int V>
+__device__ __forceinline__ void store_tile(uint16_t *dst, const float *v) {
+#pragma unroll
+    for (int j = 0; j < V / 16; ++j) {
+        float w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[16 * j + 2 * k]));
+            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[16 * j + 2 * k + 1]));
+            w[k] = __uint_as_float(lo | (hi << 16));
+        }
+        stg256(dst + 16 * j, w);
+    }
+}
+
+struct PairSched {
+    int rb_per_batch;          // row blocks of 32 rows per batch
+    int total_rb;              // batch * rb_per_batch
+    int n_seg;                 // time segments per row block
+    int seg_len;               // steps per segment (multiple of TL)
+    long long units;           // total_rb * n_seg
+    unsigned long long *counter;
+    unsigned long long *flags;  // per row block: epoch << 16 | segments done
+    float *carry;               // per row block: 32 rows x 16 states
+    const float *BC;            // packed fp32 B/C
+    unsigned long long epoch;
+};
+
+// ---------------------------------------------------------------- the scan
+
+template <typename Tin, typename Tout, int TL, int S>
+__global__ void __launch_bounds__(32, SS_PAIR_MINB)
+    scan_pair_kernel(const __grid_constant__ CUtensorMap tm_bc, const ssh::ScanParams p,
+                     const PairSched sch) {
+    using LY = PairLayout<Tin, TL, S>;
+    constexpr unsigned FULL = 0xffffffffu;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + LY::OFF_BAR);
+
+    const int lane = threadIdx.x;
+    const int q = lane & 1;              // which half of the states
+    const int L = (int)p.seqlen;
+    const bool has_z = p.z != nullptr;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    long long gt = 0;  // tiles issued by this warp so far, across units (stage/parity clock)
+    bool failed = false;
+
+    for (;;) {
+        unsigned long long t = 0;
+        if (lane == 0) t = atomicAdd(sch.counter, 1ull);
+        t = __shfl_sync(FULL, t, 0);
+        if ((long long)t >= sch.units) break;
+        const int seg = (int)(t / sch.total_rb), rbi = (int)(t % sch.total_rb);
+        const int b = rbi / sch.rb_per_batch, blk = rbi % sch.rb_per_batch;
+        const int d = blk * 32 + lane;
+        const bool row_ok = d < p.dim;
+        const int dc = row_ok ? d : p.dim - 1;
+        const long long row = (long long)b * p.dim + dc;
+        const int dp = __shfl_xor_sync(FULL, dc, 1);  // partner row (same batch)
+        const int l_begin = seg * sch.seg_len;
+        const int l_end = min(L, l_begin + sch.seg_len);
+        const int n_tiles = (l_end - l_begin + TL - 1) / TL;
+
+        // states [8q, 8q+8) of [0] the own row and [1] the partner row, as pairs
+        f2 A2[2][4], h[2][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = 8 * q + 2 * j;
+            A2[0][j] = mk2(p.A[(long long)dc * kN + n] * kLog2e, p.A[(long long)dc * kN + n + 1] * kLog2e);
+            A2[1][j] = mk2(p.A[(long long)dp * kN + n] * kLog2e, p.A[(long long)dp * kN + n + 1] * kLog2e);
+        }
+        // initial state: from h0 (first segment) or from the carry of the previous segment
+        {
+            const float *src0 = nullptr, *src1 = nullptr;
+            bool from_carry = false;
+            if (seg == 0) {
+                if (p.h0) {
+                    src0 = p.h0 + row * kN;
+                    src1 = p.h0 + ((long long)b * p.dim + dp) * kN;
+                }
+            } else {
+                const unsigned long long want = (sch.epoch << 16) | (unsigned long long)seg;
+                bool ok = true;
+                if (lane == 0) {
+                    ok = false;
+                    for (uint32_t i = 0; i < p.wait_limit; ++i) {
+                        if (ld_acquire(sch.flags + rbi) >= want) {
+                            ok = true;
+                            break;
+                        }
+                        __nanosleep(128);
+                    }
+                }
+                ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                if (!ok) {
+                    if (lane == 0) set_error(p.err, SS_ERR_TIMEOUT);
+                    failed = true;
+                    break;
+                }
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                src0 = sch.carry + ((long long)rbi * 32 + lane) * kN;
+                src1 = sch.carry + ((long long)rbi * 32 + (lane ^ 1)) * kN;
+                from_carry = true;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = 8 * q + 2 * j;
+                if (src0) {
+                    h[0][j] = from_carry ? mk2(__ldcg(src0 + n), __ldcg(src0 + n + 1))
+                                         : mk2(src0[n], src0[n + 1]);
+                    h[1][j] = from_carry ? mk2(__ldcg(src1 + n), __ldcg(src1 + n + 1))
+                                         : mk2(src1[n], src1[n + 1]);
+                } else {
+                    h[0][j] = h[1][j] = mk2(0.f, 0.f);
+                }
+            }
+        }
+        const float bias = p.bias ? p.bias[dc] : 0.f;
+        const float Dd = p.D ? p.D[dc] : 0.f;
+        const Tin *g_u = static_cast<const Tin *>(p.u) + row * L;
+        const Tin *g_dl = static_cast<const Tin *>(p.delta) + row * L;
+        const Tin *g_z = has_z ? static_cast<const Tin *>(p.z) + row * L : g_u;
+
+        // B/C tile k of this unit into ring stage (gt + k) % S
+        auto issue_bc = [&](int k) {
+            if (k < n_tiles && lane == 0 && (int)(gt + k) != p.drop_tile) {
+                const int s = (int)((gt + k) % S);
+                mbar_expect_tx(&bar[s], LY::BC_BOX);
+                tma_load_2d(smem + s * LY::BC_BOX, &tm_bc, 0,
+                            (int)((long long)b * L + l_begin + k * TL), &bar[s]);
+            }
+        };
+        // this lane's u, delta, z for tile k: whole 32-byte sectors of its row
+        auto load_streams = [&](int k, u8v (&su)[LY::NV], u8v (&sd)[LY::NV], u8v (&sz)[LY::NV]) {
+            const long long off = (long long)l_begin + (long long)k * TL;
+#pragma unroll
+            for (int v = 0; v < LY::NV; ++v) {
+                su[v] = ldg256(g_u + off + v * (32 / LY::ESZ));
+                sd[v] = ldg256(g_dl + off + v * (32 / LY::ESZ));
+                if (has_z) sz[v] = ldg256(g_z + off + v * (32 / LY::ESZ));
+            }
+        };
+
+#pragma unroll
+        for (int k = 0; k < S - 1; ++k) issue_bc(k);
+        u8v nu[LY::NV], nd[LY::NV], nz[LY::NV];
+        load_streams(0, nu, nd, nz);
+
+        for (int k = 0; k < n_tiles; ++k) {
+            issue_bc(k + S - 1);
+            u8v cu[LY::NV], cd[LY::NV], cz[LY::NV];
+#pragma unroll
+            for (int v = 0; v < LY::NV; ++v) cu[v] = nu[v], cd[v] = nd[v], cz[v] = nz[v];
+            if (k + 1 < n_tiles) load_streams(k + 1, nu, nd, nz);
+            const uint32_t *uw = cu[0].w, *dw = cd[0].w, *zw = cz[0].w;
+            // (for fp32 inputs the NV loads of a tensor are consecutive registers)
+
+            // own row: dt and dt*u for the tile (each (row, step) once)
+            f2 dt[TL / 2], du[TL / 2];
+#pragma unroll
+            for (int i = 0; i < TL / 2; ++i) {
+                const f2 x = fadd2(pair_at(dw, i, Tin()), mk2(bias, bias));
+                dt[i] = p.softplus ? softplus2_d6(x) : x;
+                du[i] = fmul2(dt[i], pair_at(uw, i, Tin()));
+            }
+
+            const long long g = gt + k;
+            const int s = (int)(g % S);
+            const bool ok = mbar_wait_bounded(&bar[s], (uint32_t)(g / S) & 1u, p.wait_limit);
+            if (!__all_sync(FULL, ok)) {
+                if (lane == 0) set_error(p.err, SS_ERR_TIMEOUT);
+                for (int j = k + 1; j < k + S && j < n_tiles; ++j)
+                    if ((int)(gt + j) != p.drop_tile)
+                        mbar_wait_bounded(&bar[(gt + j) % S], (uint32_t)((gt + j) / S) & 1u,
+                                          p.wait_limit);
+                failed = true;
+                break;
+            }
+            const float *bc = reinterpret_cast<const float *>(smem + s * LY::BC_BOX);
+
+            // the recurrence for both rows of the pair, this lane's 8 states
+            float out[TL];
+#pragma unroll
+            for (int l = 0; l < TL; ++l) {
+                const float dto = (l & 1) ? dt[l / 2].y : dt[l / 2].x;
+                const float duo = (l & 1) ? du[l / 2].y : du[l / 2].x;
+                const float dtp = __shfl_xor_sync(FULL, dto, 1);
+                const float dup = __shfl_xor_sync(FULL, duo, 1);
+                const float4 *bl = reinterpret_cast<const float4 *>(bc + l * 2 * kN + 8 * q);
+                const float4 *cl = reinterpret_cast<const float4 *>(bc + l * 2 * kN + kN + 8 * q);
+                const float4 b0 = bl[0], b1 = bl[1], c0 = cl[0], c1 = cl[1];
+                const f2 Bp[4] = {mk2(b0.x, b0.y), mk2(b0.z, b0.w), mk2(b1.x, b1.y), mk2(b1.z, b1.w)};
+                const f2 Cp[4] = {mk2(c0.x, c0.y), mk2(c0.z, c0.w), mk2(c1.x, c1.y), mk2(c1.z, c1.w)};
+                float part[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float dtr = r ? dtp : dto, dur = r ? dup : duo;
+                    const f2 dd = mk2(dtr, dtr), uu = mk2(dur, dur);
+                    f2 a0, a1;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const f2 tt = fmul2(dd, A2[r][j]);
+                        const f2 e = mk2(ex2(tt.x), ex2(tt.y));
+                        h[r][j] = ffma2(e, h[r][j], fmul2(uu, Bp[j]));
+                        if (j == 0) a0 = fmul2(Cp[0], h[r][0]);
+                        else if (j == 1) a1 = fmul2(Cp[1], h[r][1]);
+                        else if (j == 2) a0 = ffma2(Cp[2], h[r][2], a0);
+                        else a1 = ffma2(Cp[3], h[r][3], a1);
+                    }
+                    const f2 a = fadd2(a0, a1);
+                    part[r] = a.x + a.y;
+                }
+                // own total = my half of my row + the partner's half of my row
+                out[l] = part[0] + __shfl_xor_sync(FULL, part[1], 1);
+            }
+
+            // own row: D skip and silu(z) gate
+#pragma unroll
+            for (int i = 0; i < TL / 2; ++i) {
+                f2 o = ffma2(mk2(Dd, Dd), pair_at(uw, i, Tin()), mk2(out[2 * i], out[2 * i + 1]));
+                if (has_z) o = fmul2(o, silu2(pair_at(zw, i, Tin())));
+                out[2 * i] = o.x;
+                out[2 * i + 1] = o.y;
+            }
+            if (row_ok) {
+                Tout *dst = static_cast<Tout *>(p.y) + row * (long long)L + l_begin + k * TL;
+                store_tile<TL>(dst, out);
+            }
+            __syncwarp();  // every lane is done with B/C stage s before it is refilled
+        }
+        if (failed) break;
+        gt += n_tiles;
+
+        // hand the state on: to the next segment through the carry buffer, or out
+        if (seg + 1 < sch.n_seg) {
+            float *c0 = sch.carry + ((long long)rbi * 32 + lane) * kN + 8 * q;
+            float *c1 = sch.carry + ((long long)rbi * 32 + (lane ^ 1)) * kN + 8 * q;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                __stcg(c0 + 2 * j, h[0][j].x);
+                __stcg(c0 + 2 * j + 1, h[0][j].y);
+                __stcg(c1 + 2 * j, h[1][j].x);
+                __stcg(c1 + 2 * j + 1, h[1][j].y);
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release(sch.flags + rbi, (sch.epoch << 16) | (unsigned long long)(seg + 1));
+        } else if (p.h_last && row_ok) {
+            float *hl = p.h_last + row * kN + 8 * q;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                reinterpret_cast<float4 *>(hl)[j] =
+                    make_float4(h[0][2 * j].x, h[0][2 * j].y, h[0][2 * j + 1].x, h[0][2 * j + 1].y);
+        }
+        // the partner half of this row's final state lives in the partner lane
+        if (seg + 1 == sch.n_seg && p.h_last) {
+            // lane q wrote states [8q, 8q+8) of its own row above; the partner row's
+            // states [8q, 8q+8) are written by the partner's owner below
+            const bool partner_ok = (blk * 32 + (lane ^ 1)) < p.dim;
+            if (partner_ok) {
+                float *hp = p.h_last + ((long long)b * p.dim + dp) * kN + 8 * q;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    reinterpret_cast<float4 *>(hp)[j] =
+                        make_float4(h[1][2 * j].x, h[1][2 * j].y, h[1][2 * j + 1].x, h[1][2 * j + 1].y);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+template <typename Tin, typename Tout, int TL, int S>
+int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st) {
+    using LY = PairLayout<Tin, TL, S>;
+    auto kern = scan_pair_kernel<Tin, Tout, TL, S>;
+    // per device, once: allow the dynamic shared memory and ask how many
+    // one-warp CTAs fit on an SM
+    static int resident[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
+    if (resident[dev] == 0) {
+        int per_sm = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, LY::TOTAL) !=
+                cudaSuccess)
+            return SS_ERR_CUDA;
+        resident[dev] = per_sm < 1 ? 1 : per_sm;
+    }
+    const long long L = p.seqlen;
+    // 1. pack B/C, reset the work counter
+    {
+        const long long n = (long long)p.batch * L;
+        bc_pack_kernel<Tin><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
+            static_cast<const Tin *>(p.B), static_cast<const Tin *>(p.C), w.bc, L, p.batch,
+            w.counter);
+    }
+    // 2. the scan
+    auto fn = encode_fn();
+    if (!fn) return SS_ERR_CUDA;
+    CUtensorMap tm;
+    const cuuint64_t dims[2] = {(cuuint64_t)(2 * kN), (cuuint64_t)((long long)p.batch * L)};
+    const cuuint64_t strides[1] = {(cuuint64_t)(2 * kN * 4)};
+    const cuuint32_t box[2] = {(cuuint32_t)(2 * kN), (cuuint32_t)TL};
+    const cuuint32_t estr[2] = {1, 1};
+    if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, w.bc, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SS_ERR_CUDA;
+    PairSched sch;
+    sch.rb_per_batch = (p.dim + 31) / 32;
+    sch.total_rb = p.batch * sch.rb_per_batch;
+    sch.n_seg = w.n_seg;
+    sch.seg_len = (int)(((L + w.n_seg - 1) / w.n_seg + TL - 1) / TL * TL);
+    sch.n_seg = (int)((L + sch.seg_len - 1) / sch.seg_len);
+    sch.units = (long long)sch.total_rb * sch.n_seg;
+    sch.counter = w.counter;
+    sch.flags = w.flags;
+    sch.carry = w.carry;
+    sch.BC = w.bc;
+    sch.epoch = w.epoch;
+    int per_sm = resident[dev];
+    if (w.warps_per_sm > 0 && w.warps_per_sm < per_sm) per_sm = w.warps_per_sm;
+    long long grid = (long long)per_sm * w.sm_count;
+    if (grid > sch.units) grid = sch.units;
+    kern<<<(unsigned)grid, 32, LY::TOTAL, st>>>(tm, p, sch);
+    return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t ssh::pair_bc_bytes(const ssh::ScanParams &p) {
+    return (size_t)p.batch * (size_t)p.seqlen * 2 * kN * sizeof(float);
+}
+size_t ssh::pair_carry_bytes(const ssh::ScanParams &p) {
+    return (size_t)p.batch * (size_t)((p.dim + 31) / 32) * 32 * kN * sizeof(float);
+}
+int ssh::pair_row_blocks(const ssh::ScanParams &p) { return p.batch * ((p.dim + 31) / 32); }
+
+bool ssh::pair_supported(const ssh::ScanParams &p) {
+    if (p.dstate != kN) return false;
+    // whole tiles only: seqlen a multiple of the tile, so every row and every
+    // tile of every tensor starts on a 32-byte boundary (given 32-byte aligned
+    // base pointers)
+    if (p.seqlen % SS_PAIR_TL != 0) return false;
+    const void *ptrs[] = {p.u, p.delta, p.z, p.y};
+    for (const void *q : ptrs)
+        if (q && (reinterpret_cast<uintptr_t>(q) & 31u) != 0) return false;
+    if ((long long)p.batch * p.seqlen >= (1LL << 31)) return false;
+    return encode_fn() != nullptr;
+}
+
+int ssh::launch_pair(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st) {
+    constexpr int TL = SS_PAIR_TL, S = SS_PAIR_S;
+    const bool ib = p.in_dtype == SS_BF16, ob = p.out_dtype == SS_BF16;
+    if (ib && ob) return launch_cfg<uint16_t, uint16_t, TL, S>(p, w, st);
+    if (ib) return launch_cfg<uint16_t, float, TL, S>(p, w, st);
+    if (ob) return launch_cfg<float, uint16_t, TL, S>(p, w, st);
+    return launch_cfg<float, float, TL, S>(p, w, st);
+}

@@ -380,12 +380,14 @@ int launch_cfg(const ssh::ScanParams &p, int max_smem, cudaStream_t st) {
     using LY = Layout<Tin, N, TPR, RPB, TL, S>;
     auto kern = scan_rows_kernel<Tin, Tout, N, TPR, RPB, TL, S>;
     if (LY::TOTAL > max_smem) return SS_ERR_UNSUPPORTED;
-    static bool attr_set = false;  // per instantiation
-    if (!attr_set) {
+    static bool attr_set[64] = {false};  // per instantiation and device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
+    if (!attr_set[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL) !=
             cudaSuccess)
             return SS_ERR_CUDA;
-        attr_set = true;
+        attr_set[dev] = true;
     }
     const bool bf = sizeof(Tin) == 2;
     const uint64_t L = (uint64_t)p.seqlen, rows = (uint64_t)p.batch * p.dim;

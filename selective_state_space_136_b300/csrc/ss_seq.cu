@@ -380,9 +380,15 @@ int launch_cfg(const ssh::ScanParams &p, int max_smem, cudaStream_t st) {
     using LY = SeqLayout<Tin, N, W, TL, S>;
     auto kern = scan_seq_kernel<Tin, Tout, N, W, TL, S>;
     if (LY::TOTAL > max_smem) return SS_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL) !=
-        cudaSuccess)
-        return SS_ERR_CUDA;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL) !=
+            cudaSuccess)
+            return SS_ERR_CUDA;
+        attr_set[dev] = true;
+    }
     const bool bf = sizeof(Tin) == 2;
     const uint64_t L = (uint64_t)p.seqlen;
     CUtensorMap tB, tC;

@@ -125,8 +125,35 @@ def test_initial_state_and_bf16_output(dt):
 
 @pytest.mark.parametrize("tpr", [1, 2, 4])
 def test_threads_per_row(tpr):
-    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=2, dim=96, seqlen=520, seed=54)
+    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=2, dim=96, seqlen=528, seed=54)
     _full_check(cfg, ss.SS_VARIANT_ROWS, tpr=tpr)
+
+
+@pytest.mark.parametrize("segments", [1, 2, 3, 7, 33])
+def test_chained_segments(segments):
+    """The chained kernel gives the same answer for any segment count (the
+    state crosses segment boundaries through the carry buffer)."""
+    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=3, dim=70, seqlen=528, seed=59)
+    inp = workloads.scan_inputs(cfg, with_h0=True)
+    t = device_inputs(inp, cfg)
+    ctx = _ctx(ss.SS_VARIANT_ROWS, 2, segments)
+    y, hl = _run(cfg, t, ctx, h0=t["h0"])
+    assert ctx.last_launch() == (ss.SS_VARIANT_ROWS, 2)
+    y_ref, h_ref = oracle_rows(inp, cfg, np.arange(cfg.rows), h0=inp["h0"])
+    check_close(y.reshape(cfg.rows, -1), y_ref, True, "y")
+    check_close(hl.reshape(cfg.rows, -1), h_ref, True, "h_last")
+
+
+def test_chained_kernel_needs_whole_tiles():
+    """seqlen not a multiple of 16: the forced chained variant reports
+    unsupported; the automatic choice falls back and stays correct."""
+    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=1, dim=64, seqlen=520, seed=60)
+    inp = workloads.scan_inputs(cfg)
+    t = device_inputs(inp, cfg)
+    with pytest.raises(ss.SSError) as ei:
+        _run(cfg, t, _ctx(ss.SS_VARIANT_ROWS, 2))
+    assert ei.value.status == ss.SS_ERR_UNSUPPORTED
+    _full_check(cfg, ss.SS_VARIANT_AUTO)
 
 
 def test_moderate_full_tensor():
@@ -255,7 +282,7 @@ def test_host_rejects_bad_arguments():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("tpr", [1, 4])
+@pytest.mark.parametrize("tpr", [1, 2, 4])
 @pytest.mark.parametrize("drop", [0, 3])
 def test_device_wait_times_out_cleanly(tpr, drop):
     """A tile whose loads are never issued makes the bounded wait run out: the
