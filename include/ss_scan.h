@@ -137,6 +137,29 @@ typedef struct {
 int ss_state_update(ss_ctx *ctx, const ss_update_args *args, ss_stream_t stream);
 
 /*
+ * Selective scan forward without any device allocation. The pages have no
+ * counterpart to this entry point: it exists for callers that may not call
+ * cudaMalloc at all (inside memory-planned or graph-captured regions, in
+ * real-time paths that must not block on the allocator, in plugins whose host
+ * owns every allocation). ss_create allocates, so no context is used.
+ *   args         : as for ss_scan_fwd; the shape must suit the chained
+ *                  pair-row kernel (dstate 16, seqlen a multiple of 16, u,
+ *                  delta, z, y 32-byte aligned) and its scratch must fit the
+ *                  library's static 8 MiB device array (roughly
+ *                  batch * seqlen * 128 B + batch * dim * 64 B + 1 KiB);
+ *                  otherwise SS_ERR_UNSUPPORTED and nothing is enqueued.
+ *   device_error : caller-owned device int that receives SS_ERR_TIMEOUT if a
+ *                  bounded device wait gives up (it is only written then);
+ *                  may be NULL.
+ * The scratch array is shared by every call on a device and keeps the last
+ * call's contents; the call clears what must start at zero. Calls that
+ * overlap on the GPU race on it: order them on one stream. The first call on
+ * a device resolves the array's address and clears it synchronously: make it
+ * before any stream capture. Returns SS_OK or an error from ss_status.
+ */
+int ss_scan_fwd_noalloc(const ss_scan_args *args, int *device_error, ss_stream_t stream);
+
+/*
  * Synchronise `stream`, then return and clear the context's device error
  * word: SS_OK when no device-side check fired since the last read,
  * SS_ERR_TIMEOUT when a bounded wait gave up, SS_ERR_CUDA if the sync failed.
