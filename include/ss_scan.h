@@ -174,9 +174,12 @@ const char *ss_status_string(int status);
  *   SS_VARIANT_ROWS    : one pass; each row's time axis is walked in order by
  *                        a small group of threads, inputs staged by TMA.
  *   SS_VARIANT_CHUNKED : the time axis is cut into segments scanned in
- *                        parallel; per-segment (decay, state) pairs are
- *                        combined by an associative scan and the segments are
- *                        re-scanned from their carried-in state.
+ *                        parallel from a zero state; per-segment (decay,
+ *                        state) pairs are combined along time by a
+ *                        warp-shuffle associative scan and the segments are
+ *                        scanned again from their carried-in state (dstate
+ *                        16, seqlen a multiple of 16). AUTO picks it when there
+ *                        are too few row blocks of 32 rows to fill the GPU.
  *   SS_VARIANT_SIMPLE  : one thread per row, plain loads; used for shapes the
  *                        staged kernels cannot take (e.g. seqlen % 8 != 0).
  * Options (ss_set_option):

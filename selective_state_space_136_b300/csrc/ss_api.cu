@@ -25,12 +25,14 @@ bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.h
 
 // Grow the context scratch to hold the chained kernel's buffers; zero it when
 // (re)allocated (the flags must start below every epoch).
-int ensure_pair_scratch(ss_ctx *ctx, const ssh::ScanParams &p, ssh::PairWork *w) {
+int ensure_pair_scratch(ss_ctx *ctx, const ssh::ScanParams &p, int n_seg, bool chunked,
+                        ssh::PairWork *w) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t flags_b = up((size_t)ssh::pair_row_blocks(p) * 8);
     const size_t carry_b = up(ssh::pair_carry_bytes(p));
     const size_t bc_b = up(ssh::pair_bc_bytes(p));
-    const size_t need = 256 + flags_b + carry_b + bc_b;
+    const size_t agg_b = chunked ? up(ssh::pair_agg_bytes(p, n_seg)) : 0;
+    const size_t need = 256 + flags_b + carry_b + bc_b + agg_b;
     if (need > ctx->scratch_bytes) {
         if (ctx->scratch) {
             if (cudaFree(ctx->scratch) != cudaSuccess) return SS_ERR_CUDA;
@@ -46,6 +48,9 @@ int ensure_pair_scratch(ss_ctx *ctx, const ssh::ScanParams &p, ssh::PairWork *w)
     w->flags = reinterpret_cast<unsigned long long *>(base + 256);
     w->carry = reinterpret_cast<float *>(base + 256 + flags_b);
     w->bc = reinterpret_cast<float *>(base + 256 + flags_b + carry_b);
+    w->hagg = chunked ? reinterpret_cast<float *>(base + 256 + flags_b + carry_b + bc_b) : nullptr;
+    w->sdt = chunked ? w->hagg + (size_t)ssh::pair_row_blocks(p) * n_seg * 32 * 16 : nullptr;
+    w->chunked = chunked;
     return SS_OK;
 }
 
@@ -227,21 +232,49 @@ int ss_scan_fwd(ss_ctx *ctx, const ss_scan_args *a, ss_stream_t stream) {
                       ctx->drop_tile};
     int variant = ctx->variant;
     const bool rows_ok = ssh::rows_supported(p) && ssh::seq_supported(p);
-    if (variant == SS_VARIANT_AUTO) variant = rows_ok ? SS_VARIANT_ROWS : SS_VARIANT_SIMPLE;
-    if (variant == SS_VARIANT_CHUNKED) return SS_ERR_UNSUPPORTED;
+    const bool pair_ok = ssh::pair_supported(p);
+    const long long resident = (long long)(ctx->warps_per_sm > 0 ? ctx->warps_per_sm : 8) *
+                               ctx->sm_count;
+    if (variant == SS_VARIANT_AUTO) {
+        // few row blocks for the machine: scan time segments in parallel
+        if (pair_ok && 2LL * ssh::pair_row_blocks(p) < resident) variant = SS_VARIANT_CHUNKED;
+        else variant = rows_ok ? SS_VARIANT_ROWS : SS_VARIANT_SIMPLE;
+    }
     if (variant == SS_VARIANT_ROWS && !rows_ok) return SS_ERR_UNSUPPORTED;
     int rc, launches = 1;
-    if (variant == SS_VARIANT_ROWS) {
+    if (variant == SS_VARIANT_CHUNKED) {
+        if (!pair_ok) return SS_ERR_UNSUPPORTED;
+        int req = ctx->segments;
+        if (req <= 0) {
+            // at least one unit per resident warp, and segments of at most 8192
+            // steps so long sequences split into many small balanced units
+            const long long rb = ssh::pair_row_blocks(p);
+            long long r = (resident + rb - 1) / rb;
+            const long long by_len = (a->seqlen + 8191) / 8192;
+            if (by_len > r) r = by_len;
+            req = (int)(r < 2 ? 2 : (r > 65535 ? 65535 : r));
+        }
+        const int n_seg = ssh::pair_segments(p, req);
+        ssh::PairWork w{};
+        if ((rc = ensure_pair_scratch(ctx, p, n_seg, true, &w)) != SS_OK) return rc;
+        w.epoch = ++ctx->epoch;
+        w.sm_count = ctx->sm_count;
+        w.warps_per_sm = ctx->warps_per_sm;
+        w.n_seg = n_seg;
+        rc = ssh::launch_pair(p, w, st);
+        launches = n_seg >= 2 ? 4 : 2;
+    } else if (variant == SS_VARIANT_ROWS) {
         int tpr = ctx->rows_tpr;
         if (tpr == 0) tpr = ssh::pair_supported(p) ? 2 : 1;
         if (tpr == 2) {
             if (!ssh::pair_supported(p)) return SS_ERR_UNSUPPORTED;
             ssh::PairWork w{};
-            if ((rc = ensure_pair_scratch(ctx, p, &w)) != SS_OK) return rc;
+            const int n_seg = ctx->segments > 0 ? ctx->segments : 4;
+            if ((rc = ensure_pair_scratch(ctx, p, n_seg, false, &w)) != SS_OK) return rc;
             w.epoch = ++ctx->epoch;
             w.sm_count = ctx->sm_count;
             w.warps_per_sm = ctx->warps_per_sm;
-            w.n_seg = ctx->segments > 0 ? ctx->segments : 4;
+            w.n_seg = n_seg;
             rc = ssh::launch_pair(p, w, st);
             launches = 2;
         } else if (tpr == 1) {

@@ -60,7 +60,10 @@ struct PairWork {
     float *bc;                       // packed fp32 B/C, pair_bc_bytes()
     float *carry;                    // pair_carry_bytes()
     unsigned long long *flags;       // one per row block, zeroed once at allocation
-    unsigned long long *counter;     // work counter, reset by the first kernel of a call
+    unsigned long long *counter;     // two work counters, reset by the first kernel of a call
+    float *hagg;                     // chunked only: pair_agg_bytes() (end states, then carries)
+    float *sdt;                      //   and the summed dt per (row block, segment)
+    bool chunked;                    // aggregate + combine + output instead of one chained pass
     unsigned long long epoch;        // strictly increasing per call on this scratch
     int n_seg;                       // time segments per row block
     int warps_per_sm;                // persistent warps per SM (0 = as many as fit)
@@ -68,6 +71,8 @@ struct PairWork {
 };
 size_t pair_bc_bytes(const ScanParams &p);
 size_t pair_carry_bytes(const ScanParams &p);
+int pair_segments(const ScanParams &p, int requested);  // actual count for a request
+size_t pair_agg_bytes(const ScanParams &p, int n_seg);
 int pair_row_blocks(const ScanParams &p);
 bool pair_supported(const ScanParams &p);
 int launch_pair(const ScanParams &p, const PairWork &w, cudaStream_t st);

@@ -47,6 +47,7 @@ DeviceSlot g_slots[kMaxDevices];
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
+
 // Layout of the array for one call: [counter][flags][carry][packed B/C].
 size_t scratch_need(const ssh::ScanParams &p, size_t *flags_b, size_t *carry_b) {
     *flags_b = up256((size_t)ssh::pair_row_blocks(p) * 8);

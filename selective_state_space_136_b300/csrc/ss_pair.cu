@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) bc_pack_kernel(const Tin *__restrict__ B,
                                                       long long L, int batch,
                                                       unsigned long long *counter) {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // (b, l)
-    if (i == 0 && counter) *counter = 0ull;
+    if (i == 0 && counter) counter[0] = counter[1] = 0ull;  // one per scan pass
     if (i >= (long long)batch * L) return;
     const long long b = i / L, l = i % L;
     const Tin *Bb = B + b * kN * L + l;
@@ -138,14 +138,83 @@ struct PairSched {
     float *carry;               // per row block: 32 rows x 16 states
     const float *BC;            // packed fp32 B/C
     unsigned long long epoch;
+    float *hagg;                // [row block][segment][32 rows][16]: end states, then carries
+    float *sdt;                 // [row block][segment][32 rows]: summed dt per segment
 };
+
+// ---------------------------------------------------------------- cross-segment carry
+
+// One warp per row. Lane g holds segment g's affine map h -> a h + b per state
+// (a = 2^(A log2(e) * summed dt), b = end state from zero); an inclusive
+// Kogge-Stone scan with up-shuffles composes the maps in time order,
+// (a1, b1) then (a2, b2) = (a2 a1, a2 b1 + b2), and applying the prefix to
+// the initial state gives the state each segment starts from. Segments are
+// taken 32 at a time with the running state carried between rounds. The
+// result overwrites the aggregate: slot g then holds the state entering
+// segment g + 1.
+__global__ void __launch_bounds__(128) carry_combine_kernel(const ssh::ScanParams p,
+                                                            const PairSched sch) {
+    constexpr unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const long long wrow = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (wrow >= (long long)sch.total_rb * 32) return;  // whole warps exit together
+    const int rbi = (int)(wrow / 32), rib = (int)(wrow % 32);
+    const int b = rbi / sch.rb_per_batch, blk = rbi % sch.rb_per_batch;
+    const int d = blk * 32 + rib;
+    const int dc = d < p.dim ? d : p.dim - 1;
+    const long long row = (long long)b * p.dim + dc;
+    float A2[kN], hc[kN];
+#pragma unroll
+    for (int n = 0; n < kN; ++n) {
+        A2[n] = p.A[(long long)dc * kN + n] * kLog2e;
+        hc[n] = p.h0 ? p.h0[row * kN + n] : 0.f;
+    }
+    const int n_agg = sch.n_seg - 1;
+    for (int g0 = 0; g0 < n_agg; g0 += 32) {
+        const int g = g0 + lane;
+        const bool valid = g < n_agg;
+        const long long slot = ((long long)rbi * sch.n_seg + g) * 32 + rib;
+        const float sd = valid ? __ldcg(sch.sdt + slot) : 0.f;
+        float a[kN], bb[kN];
+#pragma unroll
+        for (int n = 0; n < kN; ++n) {
+            a[n] = valid ? ex2(A2[n] * sd) : 1.f;
+            bb[n] = valid ? __ldcg(sch.hagg + slot * kN + n) : 0.f;
+        }
+#pragma unroll
+        for (int off = 1; off < 32; off *= 2) {
+#pragma unroll
+            for (int n = 0; n < kN; ++n) {
+                const float ap = __shfl_up_sync(FULL, a[n], off);
+                const float bp = __shfl_up_sync(FULL, bb[n], off);
+                if (lane >= off) {
+                    bb[n] = fmaf(a[n], bp, bb[n]);
+                    a[n] *= ap;
+                }
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < kN; ++n) {
+            const float st = fmaf(a[n], hc[n], bb[n]);  // state after segment g
+            if (valid) __stcg(sch.hagg + slot * kN + n, st);
+            hc[n] = __shfl_sync(FULL, st, 31);
+        }
+    }
+}
 
 // ---------------------------------------------------------------- the scan
 
-template <typename Tin, typename Tout, int TL, int S>
+// MODE: kChain  - units chained along time through the carry buffer (one pass);
+//       kAgg    - aggregate pass: every segment but the last from a zero state,
+//                 no output; stores the end state and the summed dt;
+//       kSeg    - output pass: every segment from its carried-in state.
+enum { kChain = 0, kAgg = 1, kSeg = 2 };
+
+template <typename Tin, typename Tout, int TL, int S, int MODE>
 __global__ void __launch_bounds__(32, SS_PAIR_MINB)
     scan_pair_kernel(const __grid_constant__ CUtensorMap tm_bc, const ssh::ScanParams p,
                      const PairSched sch) {
+    constexpr bool OUT = MODE != kAgg;  // produces y
     using LY = PairLayout<Tin, TL, S>;
     constexpr unsigned FULL = 0xffffffffu;
 
@@ -171,7 +240,7 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
 
     for (;;) {
         unsigned long long t = 0;
-        if (lane == 0) t = atomicAdd(sch.counter, 1ull);
+        if (lane == 0) t = atomicAdd(sch.counter + (MODE == kSeg ? 1 : 0), 1ull);
         t = __shfl_sync(FULL, t, 0);
         if ((long long)t >= sch.units) break;
         const int seg = (int)(t / sch.total_rb), rbi = (int)(t % sch.total_rb);
@@ -193,11 +262,18 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
             A2[0][j] = mk2(p.A[(long long)dc * kN + n] * kLog2e, p.A[(long long)dc * kN + n + 1] * kLog2e);
             A2[1][j] = mk2(p.A[(long long)dp * kN + n] * kLog2e, p.A[(long long)dp * kN + n + 1] * kLog2e);
         }
-        // initial state: from h0 (first segment) or from the carry of the previous segment
+        // initial state: zero (aggregate pass), h0 (first segment), the
+        // carried-in state of the combine pass, or the chained carry
         {
             const float *src0 = nullptr, *src1 = nullptr;
             bool from_carry = false;
-            if (seg == 0) {
+            if (MODE == kAgg) {
+                // from zero
+            } else if (MODE == kSeg && seg > 0) {
+                src0 = sch.hagg + (((long long)rbi * sch.n_seg + seg - 1) * 32 + lane) * kN;
+                src1 = sch.hagg + (((long long)rbi * sch.n_seg + seg - 1) * 32 + (lane ^ 1)) * kN;
+                from_carry = true;
+            } else if (seg == 0) {
                 if (p.h0) {
                     src0 = p.h0 + row * kN;
                     src1 = p.h0 + ((long long)b * p.dim + dp) * kN;
@@ -244,6 +320,7 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
         const Tin *g_u = static_cast<const Tin *>(p.u) + row * L;
         const Tin *g_dl = static_cast<const Tin *>(p.delta) + row * L;
         const Tin *g_z = has_z ? static_cast<const Tin *>(p.z) + row * L : g_u;
+        float sdt = 0.f, sdt_c = 0.f;  // summed dt of the own row (aggregate pass), compensated
 
         // B/C tile k of this unit into ring stage (gt + k) % S
         auto issue_bc = [&](int k) {
@@ -261,7 +338,7 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
             for (int v = 0; v < LY::NV; ++v) {
                 su[v] = ldg256(g_u + off + v * (32 / LY::ESZ));
                 sd[v] = ldg256(g_dl + off + v * (32 / LY::ESZ));
-                if (has_z) sz[v] = ldg256(g_z + off + v * (32 / LY::ESZ));
+                if (OUT && has_z) sz[v] = ldg256(g_z + off + v * (32 / LY::ESZ));
             }
         };
 
@@ -277,6 +354,7 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
             for (int v = 0; v < LY::NV; ++v) cu[v] = nu[v], cd[v] = nd[v], cz[v] = nz[v];
             if (k + 1 < n_tiles) load_streams(k + 1, nu, nd, nz);
             const uint32_t *uw = cu[0].w, *dw = cd[0].w, *zw = cz[0].w;
+            (void)zw;
             // (for fp32 inputs the NV loads of a tensor are consecutive registers)
 
             // own row: dt and dt*u for the tile (each (row, step) once)
@@ -286,6 +364,20 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
                 const f2 x = fadd2(pair_at(dw, i, Tin()), mk2(bias, bias));
                 dt[i] = p.softplus ? softplus2_d6(x) : x;
                 du[i] = fmul2(dt[i], pair_at(uw, i, Tin()));
+            }
+            if (MODE == kAgg) {
+                // pairwise sum of the tile's dt, then a compensated running sum
+                f2 s4[TL / 4];
+#pragma unroll
+                for (int i = 0; i < TL / 4; ++i) s4[i] = fadd2(dt[2 * i], dt[2 * i + 1]);
+#pragma unroll
+                for (int w = TL / 8; w >= 1; w /= 2)
+#pragma unroll
+                    for (int i = 0; i < w; ++i) s4[i] = fadd2(s4[i], s4[i + w]);
+                const float ts = s4[0].x + s4[0].y;
+                const float yk = ts - sdt_c, tk = sdt + yk;
+                sdt_c = (tk - sdt) - yk;
+                sdt = tk;
             }
 
             const long long g = gt + k;
@@ -304,6 +396,29 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
 
             // the recurrence for both rows of the pair, this lane's 8 states
             float out[TL];
+            if constexpr (!OUT) {
+#pragma unroll
+                for (int l = 0; l < TL; ++l) {
+                    const float dto = (l & 1) ? dt[l / 2].y : dt[l / 2].x;
+                    const float duo = (l & 1) ? du[l / 2].y : du[l / 2].x;
+                    const float dtp = __shfl_xor_sync(FULL, dto, 1);
+                    const float dup = __shfl_xor_sync(FULL, duo, 1);
+                    const float4 *bl = reinterpret_cast<const float4 *>(bc + l * 2 * kN + 8 * q);
+                    const float4 b0 = bl[0], b1 = bl[1];
+                    const f2 Bp[4] = {mk2(b0.x, b0.y), mk2(b0.z, b0.w), mk2(b1.x, b1.y), mk2(b1.z, b1.w)};
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float dtr = r ? dtp : dto, dur = r ? dup : duo;
+                        const f2 dd = mk2(dtr, dtr), uu = mk2(dur, dur);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const f2 tt = fmul2(dd, A2[r][j]);
+                            const f2 e = mk2(ex2(tt.x), ex2(tt.y));
+                            h[r][j] = ffma2(e, h[r][j], fmul2(uu, Bp[j]));
+                        }
+                    }
+                }
+            } else {
 #pragma unroll
             for (int l = 0; l < TL; ++l) {
                 const float dto = (l & 1) ? dt[l / 2].y : dt[l / 2].x;
@@ -350,13 +465,29 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
                 Tout *dst = static_cast<Tout *>(p.y) + row * (long long)L + l_begin + k * TL;
                 store_tile<TL>(dst, out);
             }
+            }  // OUT
             __syncwarp();  // every lane is done with B/C stage s before it is refilled
         }
         if (failed) break;
         gt += n_tiles;
 
+        if (MODE == kAgg) {
+            // the segment's end state (from zero) and the own row's summed dt
+            float *a0 = sch.hagg + (((long long)rbi * sch.n_seg + seg) * 32 + lane) * kN + 8 * q;
+            float *a1 = sch.hagg + (((long long)rbi * sch.n_seg + seg) * 32 + (lane ^ 1)) * kN + 8 * q;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                __stcg(a0 + 2 * j, h[0][j].x);
+                __stcg(a0 + 2 * j + 1, h[0][j].y);
+                __stcg(a1 + 2 * j, h[1][j].x);
+                __stcg(a1 + 2 * j + 1, h[1][j].y);
+            }
+            __stcg(sch.sdt + ((long long)rbi * sch.n_seg + seg) * 32 + lane, sdt);
+            continue;
+        }
+        if (MODE == kSeg && seg + 1 < sch.n_seg) continue;
         // hand the state on: to the next segment through the carry buffer, or out
-        if (seg + 1 < sch.n_seg) {
+        if (MODE == kChain && seg + 1 < sch.n_seg) {
             float *c0 = sch.carry + ((long long)rbi * 32 + lane) * kN + 8 * q;
             float *c1 = sch.carry + ((long long)rbi * 32 + (lane ^ 1)) * kN + 8 * q;
 #pragma unroll
@@ -407,33 +538,54 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <typename Tin, typename Tout, int TL, int S>
-int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st) {
-    using LY = PairLayout<Tin, TL, S>;
-    auto kern = scan_pair_kernel<Tin, Tout, TL, S>;
-    // per device, once: allow the dynamic shared memory and ask how many
-    // one-warp CTAs fit on an SM
-    static int resident[64] = {0};
+// Per device and instantiation, once: allow the dynamic shared memory and ask
+// how many one-warp CTAs of the kernel fit on an SM.
+template <typename K>
+int resident_ctas(K kern, int smem, int *out) {
+    static int cache[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
-    if (resident[dev] == 0) {
+    if (cache[dev] == 0) {
         int per_sm = 0;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL) !=
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                 cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, LY::TOTAL) !=
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, smem) !=
                 cudaSuccess)
             return SS_ERR_CUDA;
-        resident[dev] = per_sm < 1 ? 1 : per_sm;
+        cache[dev] = per_sm < 1 ? 1 : per_sm;
     }
+    *out = cache[dev];
+    return SS_OK;
+}
+
+template <typename Tin, typename Tout, int TL, int S, int MODE>
+int launch_mode(const ssh::ScanParams &p, const ssh::PairWork &w, const PairSched &sch,
+                const CUtensorMap &tm, long long units, cudaStream_t st) {
+    using LY = PairLayout<Tin, TL, S>;
+    auto kern = scan_pair_kernel<Tin, Tout, TL, S, MODE>;
+    int per_sm = 0;
+    int rc = resident_ctas(kern, LY::TOTAL, &per_sm);
+    if (rc != SS_OK) return rc;
+    if (w.warps_per_sm > 0 && w.warps_per_sm < per_sm) per_sm = w.warps_per_sm;
+    long long grid = (long long)per_sm * w.sm_count;
+    if (grid > units) grid = units;
+    if (grid < 1) return SS_OK;
+    PairSched sc = sch;
+    sc.units = units;
+    kern<<<(unsigned)grid, 32, LY::TOTAL, st>>>(tm, p, sc);
+    return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+template <typename Tin, typename Tout, int TL, int S>
+int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st) {
     const long long L = p.seqlen;
-    // 1. pack B/C, reset the work counter
+    // 1. pack B/C, reset the work counters
     {
         const long long n = (long long)p.batch * L;
         bc_pack_kernel<Tin><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
             static_cast<const Tin *>(p.B), static_cast<const Tin *>(p.C), w.bc, L, p.batch,
             w.counter);
     }
-    // 2. the scan
     auto fn = encode_fn();
     if (!fn) return SS_ERR_CUDA;
     CUtensorMap tm;
@@ -445,30 +597,51 @@ int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return SS_ERR_CUDA;
-    PairSched sch;
+    PairSched sch{};
     sch.rb_per_batch = (p.dim + 31) / 32;
     sch.total_rb = p.batch * sch.rb_per_batch;
-    sch.n_seg = w.n_seg;
     sch.seg_len = (int)(((L + w.n_seg - 1) / w.n_seg + TL - 1) / TL * TL);
     sch.n_seg = (int)((L + sch.seg_len - 1) / sch.seg_len);
-    sch.units = (long long)sch.total_rb * sch.n_seg;
     sch.counter = w.counter;
     sch.flags = w.flags;
     sch.carry = w.carry;
     sch.BC = w.bc;
     sch.epoch = w.epoch;
-    int per_sm = resident[dev];
-    if (w.warps_per_sm > 0 && w.warps_per_sm < per_sm) per_sm = w.warps_per_sm;
-    long long grid = (long long)per_sm * w.sm_count;
-    if (grid > sch.units) grid = sch.units;
-    kern<<<(unsigned)grid, 32, LY::TOTAL, st>>>(tm, p, sch);
-    return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    sch.hagg = w.hagg;
+    sch.sdt = w.sdt;
+    if (!w.chunked || sch.n_seg < 2) {
+        // 2. one chained pass
+        return launch_mode<Tin, Tout, TL, S, kChain>(p, w, sch, tm,
+                                                     (long long)sch.total_rb * sch.n_seg, st);
+    }
+    // 2. aggregate every segment but the last, in parallel
+    int rc = launch_mode<Tin, Tout, TL, S, kAgg>(p, w, sch, tm,
+                                                 (long long)sch.total_rb * (sch.n_seg - 1), st);
+    if (rc != SS_OK) return rc;
+    // 3. combine the segment maps along time: the state entering each segment
+    {
+        const long long warps = (long long)sch.total_rb * 32;
+        carry_combine_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, st>>>(p, sch);
+        if (cudaPeekAtLastError() != cudaSuccess) return SS_ERR_CUDA;
+    }
+    // 4. every segment again from its carried-in state, writing y
+    return launch_mode<Tin, Tout, TL, S, kSeg>(p, w, sch, tm,
+                                               (long long)sch.total_rb * sch.n_seg, st);
 }
 
 }  // namespace
 
 size_t ssh::pair_bc_bytes(const ssh::ScanParams &p) {
     return (size_t)p.batch * (size_t)p.seqlen * 2 * kN * sizeof(float);
+}
+int ssh::pair_segments(const ssh::ScanParams &p, int requested) {
+    const long long tl = SS_PAIR_TL;
+    const long long seg_len = ((p.seqlen + requested - 1) / requested + tl - 1) / tl * tl;
+    return (int)((p.seqlen + seg_len - 1) / seg_len);
+}
+size_t ssh::pair_agg_bytes(const ssh::ScanParams &p, int n_seg) {
+    // end states and summed dt per (row block, segment)
+    return (size_t)ssh::pair_row_blocks(p) * (size_t)n_seg * 32 * (kN + 1) * sizeof(float);
 }
 size_t ssh::pair_carry_bytes(const ssh::ScanParams &p) {
     return (size_t)p.batch * (size_t)((p.dim + 31) / 32) * 32 * kN * sizeof(float);

@@ -144,6 +144,39 @@ def test_chained_segments(segments):
     check_close(hl.reshape(cfg.rows, -1), h_ref, True, "h_last")
 
 
+@pytest.mark.parametrize("segments,dt,dim", [(2, "bf16", 64), (3, "f32", 70), (33, "bf16", 33),
+                                             (40, "bf16", 96), (0, "bf16", 160)])
+def test_chunked_variant(segments, dt, dim):
+    """Segments scanned in parallel, carries combined by the shuffle scan,
+    segments re-scanned: same answer as the oracle for any segment count
+    (33 and 40 need two combine rounds of 32 segments)."""
+    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=2, dim=dim, seqlen=640,
+                           in_dtype=dt, seed=61 + segments)
+    inp = workloads.scan_inputs(cfg, with_h0=True)
+    t = device_inputs(inp, cfg)
+    ctx = _ctx(ss.SS_VARIANT_CHUNKED, 0, segments)
+    for h0 in (t["h0"], None):
+        y, hl = _run(cfg, t, ctx, h0=h0)
+        assert ctx.last_launch()[0] == ss.SS_VARIANT_CHUNKED
+        y_ref, h_ref = oracle_rows(inp, cfg, np.arange(cfg.rows),
+                                   h0=inp["h0"] if h0 is not None else None)
+        check_close(y.reshape(cfg.rows, -1), y_ref, dt == "bf16", "y")
+        check_close(hl.reshape(cfg.rows, -1), h_ref, dt == "bf16", "h_last")
+
+
+def test_chunked_long_memory():
+    """Tiny time steps (bias -> dt ~ 1e-5): the state carries across every
+    segment boundary, so a wrong carry shows up at once."""
+    cfg = workloads.scaled(workloads.CONFIGS["long1m"], batch=1, dim=64, seqlen=4096, seed=62,
+                           dt_lo=1e-5, dt_hi=1e-4)
+    inp = workloads.scan_inputs(cfg)
+    t = device_inputs(inp, cfg)
+    y, hl = _run(cfg, t, _ctx(ss.SS_VARIANT_CHUNKED, 0, 16))
+    y_ref, h_ref = oracle_rows(inp, cfg, np.arange(cfg.rows))
+    check_close(y.reshape(cfg.rows, -1), y_ref, True, "y")
+    check_close(hl.reshape(cfg.rows, -1), h_ref, True, "h_last")
+
+
 def test_chained_kernel_needs_whole_tiles():
     """seqlen not a multiple of 16: the forced chained variant reports
     unsupported; the automatic choice falls back and stays correct."""
@@ -282,7 +315,7 @@ def test_host_rejects_bad_arguments():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("tpr", [1, 2, 4])
+@pytest.mark.parametrize("tpr", [1, 2, 4, "chunked"])
 @pytest.mark.parametrize("drop", [0, 3])
 def test_device_wait_times_out_cleanly(tpr, drop):
     """A tile whose loads are never issued makes the bounded wait run out: the
@@ -290,7 +323,10 @@ def test_device_wait_times_out_cleanly(tpr, drop):
     cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=1, dim=64, seqlen=256, seed=58)
     inp = workloads.scan_inputs(cfg)
     t = device_inputs(inp, cfg)
-    ctx = _ctx(ss.SS_VARIANT_ROWS, tpr)
+    if tpr == "chunked":
+        ctx = _ctx(ss.SS_VARIANT_CHUNKED, 0, 2)
+    else:
+        ctx = _ctx(ss.SS_VARIANT_ROWS, tpr)
     ctx.set_option(ss.SS_OPT_WAIT_LIMIT, 2000)
     ctx.set_option(ss.SS_OPT_TEST_DROP_TILE, drop)
     ss.ss_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"],
