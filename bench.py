@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--skip-e2e", action="store_true", help="skip the host-buffer e2e leg")
     ap.add_argument("--skip-probe", action="store_true", help="skip the ALU-rate probes")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--skip-decode", action="store_true", help="skip the decode-step leg")
     return ap.parse_args()
 
 
@@ -96,30 +97,38 @@ def measured_peaks():
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def time_oracle(cfg, seconds, threads):
-    """Time the fp64 oracle on as many rows of cfg as fit in about `seconds`.
-    Returns (elements/s, rows, L, elapsed)."""
+_ORACLE_BLOCKS = {}
+
+
+def time_oracle(cfg, seconds, threads, max_blocks=2):
+    """Time the fp64 oracle on cfg's rows for about `seconds` of host time.
+
+    The sample is the first `max_blocks` blocks of up to 4096 rows (every row
+    at full length L); they are scanned in turn, repeatedly, until the timed
+    total passes `seconds`. Inputs are generated once per block, outside the
+    timed region. Returns (elements/s, row scans timed, distinct rows, elapsed)."""
     import oracle
     oracle.build()
-
-    def run(rows):
-        inp = workloads.scan_inputs(cfg, rows=rows)
+    block = max(1, min(cfg.rows, 4096))
+    starts = list(range(0, min(cfg.rows, block * max_blocks), block))
+    timed, done, i = 0.0, 0, 0
+    while True:
+        key = (cfg.name, starts[i % len(starts)])
+        if key not in _ORACLE_BLOCKS:
+            rows = np.arange(key[1], min(key[1] + block, cfg.rows))
+            _ORACLE_BLOCKS[key] = (rows, workloads.scan_inputs(cfg, rows=rows))
+        rows, inp = _ORACLE_BLOCKS[key]
         t0 = time.perf_counter()
         oracle.scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], D=inp["D"],
                         delta_bias=inp["delta_bias"], z=inp["z"], rows=rows, dim=cfg.dim,
                         threads=threads)
-        return time.perf_counter() - t0
-
-    g = np.random.default_rng(0)
-    calib = max(threads, 8)
-    rows = np.sort(g.choice(cfg.rows, size=min(calib, cfg.rows), replace=False))
-    t = run(rows)
-    per_row = t / len(rows)
-    n = int(min(cfg.rows, max(len(rows), seconds / max(per_row, 1e-9) * 1.0)))
-    n = max(threads, (n // threads) * threads) if n >= threads else n
-    rows = np.sort(g.choice(cfg.rows, size=min(n, cfg.rows), replace=False))
-    t = run(rows)
-    return len(rows) * cfg.seqlen / t, len(rows), cfg.seqlen, t
+        timed += time.perf_counter() - t0
+        done += len(rows)
+        i += 1
+        if timed >= seconds:
+            break
+    distinct = min(cfg.rows, block * len(starts))
+    return done * cfg.seqlen / timed, done, distinct, timed
 
 
 # ---------------------------------------------------------------- clocks
@@ -199,14 +208,14 @@ def probe_alu(device):
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("ss_rows.cu", "ss_common.cuh"):
+    for f in ("ss_pair.cu", "ss_common.cuh"):
         h.update(open(os.path.join(ROOT, "selective_state_space_136_b300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def committed_traffic(cfg_name):
     """dram bytes per launch recorded in profiles/, if taken on this exact source."""
-    p = os.path.join(ROOT, "profiles", "ncu_scan_rows_%s.md" % cfg_name)
+    p = os.path.join(ROOT, "profiles", "ncu_scan_pair_%s.md" % cfg_name)
     if not os.path.exists(p):
         return None
     sha, traffic = None, None
@@ -222,6 +231,72 @@ def committed_traffic(cfg_name):
 
 
 # ---------------------------------------------------------------- our arm
+
+def workload_config(cfg):
+    """The `config` keys both arms share: the workload and its sizes."""
+    return {"workload": "%s: batch %d, d_inner %d, d_state %d, L %d, %s u/delta/z/B/C, "
+                        "fp32 state/y, z gate + D skip, h_last out"
+                        % (cfg.name, cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen, cfg.in_dtype),
+            "batch": cfg.batch, "d_inner": cfg.dim, "d_state": cfg.dstate,
+            "seq_len": cfg.seqlen, "in_dtype": cfg.in_dtype, "out_dtype": "f32"}
+
+
+def time_decode(ss, ctx, dev, stream, args, n_sets=6):
+    """Time ss_state_update on the decode workload (batch 128, d_inner 5120,
+    d_state 16, bf16 x/dt/z/B/C, fp32 state in place, fp32 y).
+
+    The 41.9 MB state fits in L2, so `n_sets` independent (state, inputs) sets
+    are cycled: between two uses of one state, the other sets move more than
+    the 126 MB of L2 through it, and every step reads its state from HBM."""
+    import torch
+    cfg = workloads.DECODE
+    prm = workloads.params(cfg)
+    A = torch.from_numpy(prm["A"]).to(dev)
+    Dp = torch.from_numpy(prm["D"]).to(dev)
+    bias = torch.from_numpy(prm["delta_bias"]).to(dev)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    sets = []
+    for k in range(n_sets):
+        st = torch.from_numpy(workloads.decode_state0(cfg)).to(dev)
+        inp = {n: bf(v).to(dev) for n, v in workloads.decode_step_inputs(cfg, k).items()}
+        y = torch.empty((cfg.batch, cfg.dim), dtype=torch.float32, device=dev)
+        sets.append((st, inp, y))
+
+    def one(k):
+        st, inp, y = sets[k % n_sets]
+        ss.ss_state_update(st, inp["x"], inp["dt"], A, inp["B"], inp["C"], D=Dp, dt_bias=bias,
+                           z=inp["z"], y=y, ctx=ctx, stream=stream)
+
+    for k in range(max(args.warmup, 3) * n_sets):
+        one(k)
+    torch.cuda.synchronize(dev)
+    steps = max(args.steps, 1) * n_sets
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(steps):
+        one(k)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ctx.device_error() != ss.SS_OK:
+        raise RuntimeError("device error in the decode leg")
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    rows = cfg.batch * cfg.dim
+    nbytes = (2 * rows * cfg.dstate * 4 + 3 * rows * 2 + 2 * cfg.batch * cfg.dstate * 2
+              + rows * 4 + cfg.dim * cfg.dstate * 4 + 2 * cfg.dim * 4)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    peak, src = measured_peaks()
+    return {"workload": "decode: batch %d, d_inner %d, d_state %d, bf16 x/dt/z/B/C, fp32 state "
+                        "in place, fp32 y; %d state sets cycled" % (cfg.batch, cfg.dim, cfg.dstate,
+                                                                    n_sets),
+            "us_per_step": us, "tokens_per_s": cfg.batch / (us * 1e-6),
+            "algorithmic_bytes_per_step": nbytes, "gbs": gbs,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "peak_source": src,
+                         "unit": "GB/s", "frac": gbs / peak},
+            "steps": steps, "gpu_launches": steps}
+
 
 def run_ours(args, rank, world, local):
     import torch
@@ -307,6 +382,8 @@ def run_ours(args, rank, world, local):
     avg_launch_s = float(np.mean(per_launch_ms)) * 1e-3
     host_us_per_call = (t_enq - t_wall0) / args.steps * 1e6
 
+    decode = None if args.skip_decode else time_decode(ss, ctx, dev, stream, args)
+
     # ---- end to end: pinned host inputs in, y and h_last back to host, every step
     e2e = None
     if not args.skip_e2e:
@@ -375,6 +452,13 @@ def run_ours(args, rank, world, local):
     for t in terms.values():
         t["frac"] = t["achieved"] / t["peak"]
     dominant = max(terms, key=lambda k: terms[k]["floor_us"])
+    # informative: the 4 FP32 lane-ops and the ex2 of a state element all take
+    # issue slots of the same warp scheduler (1 warp-instruction per clock per
+    # scheduler, 4 schedulers per SM), so 5 slots per 32 elements bound the
+    # arithmetic before any overhead; not part of the max above
+    issue_floor_us = bdln * 5 / 32 / (4 * sms) / (MAX_SM_MHZ * 1e6) * 1e6
+    issue_term = {"floor_us": issue_floor_us, "frac": issue_floor_us / (avg_launch_s * 1e6),
+                  "note": "5 issue slots (4 FP32 + 1 MUFU) per 32 state elements, 4 schedulers/SM"}
     dt = terms[dominant]
     roofline = {"bound": "hbm" if dominant == "hbm" else "alu", "term": dominant,
                 "achieved": dt["achieved"], "peak": dt["peak"], "unit": dt["unit"],
@@ -385,15 +469,16 @@ def run_ours(args, rank, world, local):
                                "events on the launching stream, averaged over the timed steps",
                 "floor_us": max(t["floor_us"] for t in terms.values()),
                 "frac_of_floor": max(t["floor_us"] for t in terms.values()) / (avg_launch_s * 1e6),
-                "terms": terms, "peak_clock_mhz": MAX_SM_MHZ}
+                "terms": terms, "issue_slots": issue_term, "peak_clock_mhz": MAX_SM_MHZ}
 
     cpu = None
     if not args.skip_cpu:
         cores = cpu_cores()
-        v, nrows, L, el = time_oracle(cfg, args.cpu_seconds, cores)
+        v, nrows, distinct, el = time_oracle(cfg, args.cpu_seconds, cores)
         cpu = {"value": v, "unit": "elements/s", "cores": cores, "kind": "oracle",
-               "sample": "%d of %d rows (b,d) x full L=%d of %s, fp64 C oracle, %.1f s"
-                         % (nrows, cfg.rows, L, args.config, el)}
+               "sample": "%d row scans at full L=%d over the first %d of the %d rows (b,d) of %s, "
+                         "repeated; %.1f s timed, fp64 C oracle"
+                         % (nrows, cfg.seqlen, distinct, cfg.rows, args.config, el)}
 
     names = {0: "auto", 1: "rows", 2: "chunked", 3: "simple"}
     out = {
@@ -401,15 +486,10 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded normal draws; A=-(n+1); dt bias log-uniform [1e-3,1e-1])",
-        "config": {"workload": "%s: batch %d, d_inner %d, d_state %d, L %d, %s u/delta/z/B/C, "
-                               "fp32 state/y, z gate + D skip, h_last out"
-                               % (cfg.name, cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen,
-                                  cfg.in_dtype),
-                   "batch": cfg.batch, "d_inner": cfg.dim, "d_state": cfg.dstate,
-                   "seq_len": cfg.seqlen, "in_dtype": cfg.in_dtype, "out_dtype": "f32",
-                   "variant": names.get(variant, str(variant)),
-                   "l2": "no flush: %.0f MB of inputs+outputs per step > 126 MB L2" % (nbytes / 1e6),
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": dict(workload_config(cfg),
+                       variant=names.get(variant, str(variant)),
+                       l2="no flush: %.0f MB of inputs+outputs per step > 126 MB L2" % (nbytes / 1e6),
+                       parallelism="replicas" if world > 1 else "single"),
         "gbs": gbs,
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -418,6 +498,7 @@ def run_ours(args, rank, world, local):
         "gpu_launches": int(args.steps * launches_per_step),
         "host_us_per_call": host_us_per_call,
         "alu_probe": probes,
+        "decode": decode,
         "impl": "ours",
     }
     print(json.dumps(out), flush=True)
@@ -435,21 +516,21 @@ def run_reference(args, rank, world):
     per_step = max(1.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         time_oracle(cfg, per_step / 4, cores)
-    vals, rows_done, secs = [], 0, 0.0
+    vals, rows_done, secs, distinct = [], 0, 0.0, 0
     for _ in range(args.steps):
-        v, nrows, L, el = time_oracle(cfg, per_step, cores)
+        v, nrows, distinct, el = time_oracle(cfg, per_step, cores)
         vals.append(v)
         rows_done += nrows
         secs += el
     value = float(np.mean(vals))
-    sample = ("per step %d-ish of %d rows x full L=%d of %s, fp64 C oracle on %d host threads"
-              % (rows_done // max(1, args.steps), cfg.rows, cfg.seqlen, args.config, cores))
+    sample = ("%d row scans at full L=%d over the first %d of the %d rows (b,d) of %s, repeated, "
+              "in %d steps; %.1f s timed, fp64 C oracle on %d host threads"
+              % (rows_done, cfg.seqlen, distinct, cfg.rows, args.config, args.steps, secs, cores))
     out = {"metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": cfg.elements / value * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": cfg.name, "batch": cfg.batch, "d_inner": cfg.dim,
-                      "d_state": cfg.dstate, "seq_len": cfg.seqlen},
+           "config": dict(workload_config(cfg), parallelism="single"),
            "impl": "reference",
            "cpu_baseline": {"value": value, "unit": "elements/s", "cores": cores,
                             "kind": "oracle", "sample": sample},
