@@ -165,6 +165,18 @@ __device__ __forceinline__ f2 softplus2(f2 x) {
 }
 
 // silu on a pair: z / (1 + 2^(-z log2 e)); z << 0 gives rcp(inf) = 0 -> -0.
+// silu(z) = z sigmoid(z) = (z/2) (1 + tanh(z/2)): one MUFU.TANH per element.
+// tanh.approx.f32 has a relative error near 2^-11, so this form serves the
+// bf16-input path only (its tolerance is relative to max |y|).
+__device__ __forceinline__ float tanh_approx(float x) {
+    float r;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ f2 silu2_tanh(f2 z) {
+    const f2 hz = fmul2(z, mk2(0.5f, 0.5f));
+    return ffma2(hz, mk2(tanh_approx(hz.x), tanh_approx(hz.y)), hz);
+}
 __device__ __forceinline__ f2 silu2(f2 z) {
     const f2 t = fmul2(z, mk2(-kLog2e, -kLog2e));
     const f2 d = fadd2(mk2(ex2(t.x), ex2(t.y)), mk2(1.f, 1.f));

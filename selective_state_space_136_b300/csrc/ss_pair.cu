@@ -28,10 +28,10 @@
 // the machine: nothing is recomputed, and the exact order of the recurrence
 // along time is kept. A segment count of 1 gives plain static rows.
 //
-// Per tile of TL steps: the own row's u, delta, z arrive by cp.async into a
-// [tensor][chunk][lane] ring (conflict-free 128-bit reads); the fp32 B/C tile
-// arrives by one TMA box into an mbarrier-tracked ring. Steps past the end of
-// the sequence get dt = 0, an exact no-op on the state.
+// Per tile of TL steps: each lane loads its own row's u, delta, z for the
+// next tile with one 256-bit load per tensor (whole 32-byte sectors, one tile
+// ahead, held in registers) and writes its y as whole sectors; the fp32 B/C
+// tile arrives by one TMA box into an mbarrier-tracked ring of S stages.
 #include "ss_common.cuh"
 #include "ss_internal.h"
 
@@ -45,6 +45,9 @@
 #endif
 #ifndef SS_PAIR_MINB
 #define SS_PAIR_MINB 8
+#endif
+#ifndef SS_PAIR_TANH
+#define SS_PAIR_TANH 1  // silu through tanh.approx for bf16 inputs
 #endif
 
 namespace {
@@ -457,7 +460,9 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
 #pragma unroll
             for (int i = 0; i < TL / 2; ++i) {
                 f2 o = ffma2(mk2(Dd, Dd), pair_at(uw, i, Tin()), mk2(out[2 * i], out[2 * i + 1]));
-                if (has_z) o = fmul2(o, silu2(pair_at(zw, i, Tin())));
+                if (has_z)
+                    o = fmul2(o, (SS_PAIR_TANH && sizeof(Tin) == 2) ? silu2_tanh(pair_at(zw, i, Tin()))
+                                                                   : silu2(pair_at(zw, i, Tin())));
                 out[2 * i] = o.x;
                 out[2 * i + 1] = o.y;
             }
