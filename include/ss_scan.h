@@ -184,15 +184,17 @@ const char *ss_status_string(int status);
  *                        staged kernels cannot take (e.g. seqlen % 8 != 0).
  * Options (ss_set_option):
  *   SS_OPT_VARIANT          one of ss_variant.
- *   SS_OPT_SEGMENTS         time segments per row block for the chained rows
- *                           variant and the chunked variant (0 = auto).
+ *   SS_OPT_SEGMENTS         time segments per row block for the chunked
+ *                           variant (0 = auto).
  *   SS_OPT_THREADS_PER_ROW  how the rows variant splits a row's states over
  *                           threads: 1 = one thread per row (any dstate);
- *                           2 = two threads share a pair of rows, time
- *                           segments chained through the context scratch
- *                           (dstate 16); 4 = four threads per row (dstate
- *                           16); 0 = auto (2 for dstate 16, else 1).
- *   SS_OPT_RESIDENT_WARPS   persistent warps per SM for the chained variant
+ *                           2 = two threads share a pair of rows, and the
+ *                           row blocks' time steps are cut into one equal
+ *                           range per persistent warp (a row block split
+ *                           between two ranges passes its state through the
+ *                           context scratch; dstate 16); 4 = four threads per
+ *                           row (dstate 16); 0 = auto (2 for dstate 16, else 1).
+ *   SS_OPT_RESIDENT_WARPS   persistent warps per SM for the pair kernel
  *                           (default 8; 0 = as many as fit).
  *   SS_OPT_WAIT_LIMIT       polls before a device-side wait gives up and
  *                           reports SS_ERR_TIMEOUT (default 2^22, roughly a

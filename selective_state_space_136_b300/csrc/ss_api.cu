@@ -269,7 +269,7 @@ int ss_scan_fwd(ss_ctx *ctx, const ss_scan_args *a, ss_stream_t stream) {
         if (tpr == 2) {
             if (!ssh::pair_supported(p)) return SS_ERR_UNSUPPORTED;
             ssh::PairWork w{};
-            const int n_seg = ctx->segments > 0 ? ctx->segments : 4;
+            const int n_seg = 1;  // the chained kernel balances by tile ranges, not segments
             if ((rc = ensure_pair_scratch(ctx, p, n_seg, false, &w)) != SS_OK) return rc;
             w.epoch = ++ctx->epoch;
             w.sm_count = ctx->sm_count;

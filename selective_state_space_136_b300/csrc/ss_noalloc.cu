@@ -128,7 +128,7 @@ extern "C" int ss_scan_fwd_noalloc(const ss_scan_args *a, int *device_error,
         std::lock_guard<std::mutex> g(slot.mu);
         w.epoch = ++slot.calls;
     }
-    w.n_seg = 4;
+    w.n_seg = 1;
     w.warps_per_sm = 8;
     w.sm_count = slot.sm_count;
     return ssh::launch_pair(p, w, reinterpret_cast<cudaStream_t>(stream));

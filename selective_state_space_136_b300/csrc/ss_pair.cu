@@ -130,20 +130,49 @@ __device__ __forceinline__ void store_tile(uint16_t *dst, const float *v) {
     }
 }
 
+// Work of one pass.
+//  chained (one pass): the tiles of all row blocks, laid end to end, are cut
+//    into `units` equal ranges (one per persistent warp, taken in order from
+//    the counter). With at least as many row blocks as ranges, a range spans
+//    at most the tail of one row block, whole row blocks, and the head of one
+//    more, so each row block is split at most once: its head piece (in one
+//    range) hands its end state to its tail piece (in the next range) through
+//    the carry buffer. This balances the work to within one tile per warp.
+//  chunked passes: units are (segment, row block) in segment-major order.
 struct PairSched {
     int rb_per_batch;          // row blocks of 32 rows per batch
     int total_rb;              // batch * rb_per_batch
-    int n_seg;                 // time segments per row block
-    int seg_len;               // steps per segment (multiple of TL)
-    long long units;           // total_rb * n_seg
+    int nt;                    // tiles per row
+    int n_seg;                 // chunked: time segments per row block
+    int seg_len;               // chunked: steps per segment (multiple of TL)
+    long long units;           // chained: ranges; chunked: segments x row blocks
     unsigned long long *counter;
-    unsigned long long *flags;  // per row block: epoch << 16 | segments done
+    unsigned long long *flags;  // per row block: epoch << 16 | 1 once its head piece is done
     float *carry;               // per row block: 32 rows x 16 states
     const float *BC;            // packed fp32 B/C
     unsigned long long epoch;
     float *hagg;                // [row block][segment][32 rows][16]: end states, then carries
     float *sdt;                 // [row block][segment][32 rows]: summed dt per segment
 };
+
+// Chained pass: store the end state of the head piece of row block `rbi`
+// (this lane's half of the states of its row pair) and release the row
+// block's flag so its tail piece may start from it.
+__device__ __forceinline__ void publish_carry(const PairSched &sch, int rbi, int lane, int q,
+                                              const f2 (&h)[2][4]) {
+    float *c0 = sch.carry + ((long long)rbi * 32 + lane) * kN + 8 * q;
+    float *c1 = sch.carry + ((long long)rbi * 32 + (lane ^ 1)) * kN + 8 * q;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        __stcg(c0 + 2 * j, h[0][j].x);
+        __stcg(c0 + 2 * j + 1, h[0][j].y);
+        __stcg(c1 + 2 * j, h[1][j].x);
+        __stcg(c1 + 2 * j + 1, h[1][j].y);
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) st_release(sch.flags + rbi, (sch.epoch << 16) | 1ull);
+}
 
 // ---------------------------------------------------------------- cross-segment carry
 
@@ -213,8 +242,14 @@ __global__ void __launch_bounds__(128) carry_combine_kernel(const ssh::ScanParam
 //       kSeg    - output pass: every segment from its carried-in state.
 enum { kChain = 0, kAgg = 1, kSeg = 2 };
 
+#ifdef SS_PAIR_MAXNREG
+#define SS_PAIR_BOUNDS __maxnreg__(SS_PAIR_MAXNREG)
+#else
+#define SS_PAIR_BOUNDS __launch_bounds__(32, SS_PAIR_MINB)
+#endif
+
 template <typename Tin, typename Tout, int TL, int S, int MODE>
-__global__ void __launch_bounds__(32, SS_PAIR_MINB)
+__global__ void SS_PAIR_BOUNDS
     scan_pair_kernel(const __grid_constant__ CUtensorMap tm_bc, const ssh::ScanParams p,
                      const PairSched sch) {
     constexpr bool OUT = MODE != kAgg;  // produces y
@@ -241,21 +276,50 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
     long long gt = 0;  // tiles issued by this warp so far, across units (stage/parity clock)
     bool failed = false;
 
+    // chained pass: ranges of the row blocks' tiles laid end to end (see PairSched)
+    long long r_begin = 0, r_end = 0, c_cur = -1, c_first = 0;
     for (;;) {
-        unsigned long long t = 0;
-        if (lane == 0) t = atomicAdd(sch.counter + (MODE == kSeg ? 1 : 0), 1ull);
-        t = __shfl_sync(FULL, t, 0);
-        if ((long long)t >= sch.units) break;
-        const int seg = (int)(t / sch.total_rb), rbi = (int)(t % sch.total_rb);
+        int seg = 0, rbi = 0, t_begin = 0, t_end = 0;  // the piece: tiles [t_begin, t_end) of row block rbi
+        if (MODE == kChain) {
+            if (c_cur < c_first) {
+                // next range; its pieces go from the last row block it touches
+                // to the first, so the head piece a later range waits for is done
+                // first and the tail piece that waits on an earlier range is done last
+                unsigned long long t = 0;
+                if (lane == 0) t = atomicAdd(sch.counter, 1ull);
+                t = __shfl_sync(FULL, t, 0);
+                if ((long long)t >= sch.units) break;
+                const long long total = (long long)sch.total_rb * sch.nt;
+                r_begin = total * (long long)t / sch.units;
+                r_end = total * ((long long)t + 1) / sch.units;
+                if (r_end <= r_begin) continue;
+                c_first = r_begin / sch.nt;
+                c_cur = (r_end - 1) / sch.nt;
+            }
+            rbi = (int)c_cur;
+            t_begin = (int)(max(r_begin, c_cur * sch.nt) - c_cur * sch.nt);
+            t_end = (int)(min(r_end, (c_cur + 1) * sch.nt) - c_cur * sch.nt);
+            --c_cur;
+        } else {
+            unsigned long long t = 0;
+            if (lane == 0) t = atomicAdd(sch.counter + (MODE == kSeg ? 1 : 0), 1ull);
+            t = __shfl_sync(FULL, t, 0);
+            if ((long long)t >= sch.units) break;
+            seg = (int)(t / sch.total_rb);
+            rbi = (int)(t % sch.total_rb);
+            t_begin = seg * (sch.seg_len / TL);
+            t_end = min(sch.nt, t_begin + sch.seg_len / TL);
+        }
         const int b = rbi / sch.rb_per_batch, blk = rbi % sch.rb_per_batch;
         const int d = blk * 32 + lane;
         const bool row_ok = d < p.dim;
         const int dc = row_ok ? d : p.dim - 1;
         const long long row = (long long)b * p.dim + dc;
         const int dp = __shfl_xor_sync(FULL, dc, 1);  // partner row (same batch)
-        const int l_begin = seg * sch.seg_len;
-        const int l_end = min(L, l_begin + sch.seg_len);
-        const int n_tiles = (l_end - l_begin + TL - 1) / TL;
+        const int l_begin = t_begin * TL;
+        const int n_tiles = t_end - t_begin;
+        // chained: where the piece's state comes from and goes to
+        const bool at_start = t_begin == 0, at_end = t_end == sch.nt;
 
         // states [8q, 8q+8) of [0] the own row and [1] the partner row, as pairs
         f2 A2[2][4], h[2][4];
@@ -276,13 +340,14 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
                 src0 = sch.hagg + (((long long)rbi * sch.n_seg + seg - 1) * 32 + lane) * kN;
                 src1 = sch.hagg + (((long long)rbi * sch.n_seg + seg - 1) * 32 + (lane ^ 1)) * kN;
                 from_carry = true;
-            } else if (seg == 0) {
+            } else if (MODE == kSeg || at_start) {
                 if (p.h0) {
                     src0 = p.h0 + row * kN;
                     src1 = p.h0 + ((long long)b * p.dim + dp) * kN;
                 }
             } else {
-                const unsigned long long want = (sch.epoch << 16) | (unsigned long long)seg;
+                // the tail of a split row block: wait for its head's carry
+                const unsigned long long want = (sch.epoch << 16) | 1ull;
                 bool ok = true;
                 if (lane == 0) {
                     ok = false;
@@ -456,6 +521,11 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
                 out[l] = part[0] + __shfl_xor_sync(FULL, part[1], 1);
             }
 
+            // chained head piece: its end state is known now; hand it on before
+            // this tile's y stores are issued, so the fence that orders the carry
+            // before the flag has no fresh stores to wait for
+            if (MODE == kChain && k + 1 == n_tiles && !at_end) publish_carry(sch, rbi, lane, q, h);
+
             // own row: D skip and silu(z) gate
 #pragma unroll
             for (int i = 0; i < TL / 2; ++i) {
@@ -490,39 +560,24 @@ __global__ void __launch_bounds__(32, SS_PAIR_MINB)
             __stcg(sch.sdt + ((long long)rbi * sch.n_seg + seg) * 32 + lane, sdt);
             continue;
         }
-        if (MODE == kSeg && seg + 1 < sch.n_seg) continue;
-        // hand the state on: to the next segment through the carry buffer, or out
-        if (MODE == kChain && seg + 1 < sch.n_seg) {
-            float *c0 = sch.carry + ((long long)rbi * 32 + lane) * kN + 8 * q;
-            float *c1 = sch.carry + ((long long)rbi * 32 + (lane ^ 1)) * kN + 8 * q;
+        // the final state, once the row block's last tile is done (a chained
+        // head piece handed its state on inside its last tile). Lane q holds
+        // states [8q, 8q+8) of its own row and of the partner row.
+        const bool last = MODE == kSeg ? seg + 1 == sch.n_seg : at_end;
+        if (last && p.h_last) {
+            if (row_ok) {
+                float *hl = p.h_last + row * kN + 8 * q;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                __stcg(c0 + 2 * j, h[0][j].x);
-                __stcg(c0 + 2 * j + 1, h[0][j].y);
-                __stcg(c1 + 2 * j, h[1][j].x);
-                __stcg(c1 + 2 * j + 1, h[1][j].y);
+                for (int j = 0; j < 2; ++j)
+                    reinterpret_cast<float4 *>(hl)[j] = make_float4(
+                        h[0][2 * j].x, h[0][2 * j].y, h[0][2 * j + 1].x, h[0][2 * j + 1].y);
             }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release(sch.flags + rbi, (sch.epoch << 16) | (unsigned long long)(seg + 1));
-        } else if (p.h_last && row_ok) {
-            float *hl = p.h_last + row * kN + 8 * q;
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-                reinterpret_cast<float4 *>(hl)[j] =
-                    make_float4(h[0][2 * j].x, h[0][2 * j].y, h[0][2 * j + 1].x, h[0][2 * j + 1].y);
-        }
-        // the partner half of this row's final state lives in the partner lane
-        if (seg + 1 == sch.n_seg && p.h_last) {
-            // lane q wrote states [8q, 8q+8) of its own row above; the partner row's
-            // states [8q, 8q+8) are written by the partner's owner below
-            const bool partner_ok = (blk * 32 + (lane ^ 1)) < p.dim;
-            if (partner_ok) {
+            if ((blk * 32 + (lane ^ 1)) < p.dim) {
                 float *hp = p.h_last + ((long long)b * p.dim + dp) * kN + 8 * q;
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
-                    reinterpret_cast<float4 *>(hp)[j] =
-                        make_float4(h[1][2 * j].x, h[1][2 * j].y, h[1][2 * j + 1].x, h[1][2 * j + 1].y);
+                    reinterpret_cast<float4 *>(hp)[j] = make_float4(
+                        h[1][2 * j].x, h[1][2 * j].y, h[1][2 * j + 1].x, h[1][2 * j + 1].y);
             }
         }
     }
@@ -576,7 +631,8 @@ int launch_mode(const ssh::ScanParams &p, const ssh::PairWork &w, const PairSche
     if (grid > units) grid = units;
     if (grid < 1) return SS_OK;
     PairSched sc = sch;
-    sc.units = units;
+    // chained: one range per warp (never more ranges than row blocks)
+    sc.units = MODE == kChain ? grid : units;
     kern<<<(unsigned)grid, 32, LY::TOTAL, st>>>(tm, p, sc);
     return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
@@ -605,6 +661,7 @@ int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st
     PairSched sch{};
     sch.rb_per_batch = (p.dim + 31) / 32;
     sch.total_rb = p.batch * sch.rb_per_batch;
+    sch.nt = (int)(L / TL);
     sch.seg_len = (int)(((L + w.n_seg - 1) / w.n_seg + TL - 1) / TL * TL);
     sch.n_seg = (int)((L + sch.seg_len - 1) / sch.seg_len);
     sch.counter = w.counter;
@@ -615,9 +672,8 @@ int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st
     sch.hagg = w.hagg;
     sch.sdt = w.sdt;
     if (!w.chunked || sch.n_seg < 2) {
-        // 2. one chained pass
-        return launch_mode<Tin, Tout, TL, S, kChain>(p, w, sch, tm,
-                                                     (long long)sch.total_rb * sch.n_seg, st);
+        // 2. one chained pass: at most one range per row block
+        return launch_mode<Tin, Tout, TL, S, kChain>(p, w, sch, tm, (long long)sch.total_rb, st);
     }
     // 2. aggregate every segment but the last, in parallel
     int rc = launch_mode<Tin, Tout, TL, S, kAgg>(p, w, sch, tm,

@@ -129,19 +129,32 @@ def test_threads_per_row(tpr):
     _full_check(cfg, ss.SS_VARIANT_ROWS, tpr=tpr)
 
 
-@pytest.mark.parametrize("segments", [1, 2, 3, 7, 33])
-def test_chained_segments(segments):
-    """The chained kernel gives the same answer for any segment count (the
-    state crosses segment boundaries through the carry buffer)."""
-    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=3, dim=70, seqlen=528, seed=59)
+@pytest.mark.parametrize("batch,dim,seqlen,warps_per_sm,dt", [
+    (3, 3200, 160, 1, "f32"),    # ~2 row blocks per warp: tail, whole block, head
+    (3, 3200, 160, 2, "bf16"),   # barely more row blocks than warps: tiny slack
+    (2, 4736, 160, 2, "f32"),    # exactly one row block per warp
+    (2, 4736, 528, 1, "bf16"),   # exactly two per warp, odd tile count
+    (3, 3190, 160, 1, "f32"),    # partial last row block of each batch
+    (1, 640, 160, 1, "f32"),     # fewer row blocks than warps
+])
+def test_chained_wraparound(batch, dim, seqlen, warps_per_sm, dt):
+    """The chained kernel cuts the row blocks' tiles, laid end to end, into
+    one equal range per warp; a row block split between two ranges passes its
+    state from its head piece to its tail piece through the carry buffer. Every
+    output and final state matches the oracle, with and without h0."""
+    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=batch, dim=dim, seqlen=seqlen,
+                           in_dtype=dt, seed=59 + dim % 97 + warps_per_sm)
     inp = workloads.scan_inputs(cfg, with_h0=True)
     t = device_inputs(inp, cfg)
-    ctx = _ctx(ss.SS_VARIANT_ROWS, 2, segments)
-    y, hl = _run(cfg, t, ctx, h0=t["h0"])
-    assert ctx.last_launch() == (ss.SS_VARIANT_ROWS, 2)
-    y_ref, h_ref = oracle_rows(inp, cfg, np.arange(cfg.rows), h0=inp["h0"])
-    check_close(y.reshape(cfg.rows, -1), y_ref, True, "y")
-    check_close(hl.reshape(cfg.rows, -1), h_ref, True, "h_last")
+    ctx = _ctx(ss.SS_VARIANT_ROWS, 2)
+    ctx.set_option(ss.SS_OPT_RESIDENT_WARPS, warps_per_sm)
+    for h0 in (t["h0"], None):
+        y, hl = _run(cfg, t, ctx, h0=h0)
+        assert ctx.last_launch() == (ss.SS_VARIANT_ROWS, 2)
+        y_ref, h_ref = oracle_rows(inp, cfg, np.arange(cfg.rows),
+                                   h0=inp["h0"] if h0 is not None else None)
+        check_close(y.reshape(cfg.rows, -1), y_ref, dt == "bf16", "y")
+        check_close(hl.reshape(cfg.rows, -1), h_ref, dt == "bf16", "h_last")
 
 
 @pytest.mark.parametrize("segments,dt,dim", [(2, "bf16", 64), (3, "f32", 70), (33, "bf16", 33),
