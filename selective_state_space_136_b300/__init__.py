@@ -214,6 +214,55 @@ def ss_scan_fwd(u, delta, A, B, C, D=None, delta_bias=None, z=None, delta_softpl
     return y, h_last
 
 
+class PreparedScan:
+    """An ss_scan_fwd call whose arguments were checked and marshalled once.
+
+    Calling it enqueues the same scan again (same tensors, context and
+    stream), with none of the per-call Python checks; for loops that run one
+    shape over buffers that stay in place. The tensors must outlive it."""
+
+    def __init__(self, u, delta, A, B, C, D=None, delta_bias=None, z=None, delta_softplus=True,
+                 h0=None, y=None, h_last=None, out_dtype=None, ctx: Context | None = None,
+                 stream=None):
+        import torch
+        self.y, self.h_last = y, h_last
+        # the one-time checks are those of ss_scan_fwd; allocate outputs the same way
+        _need(u, "u")
+        batch, dim, L = u.shape
+        N = B.shape[1]
+        dev = u.device
+        _need(delta, "delta", u.shape, u.dtype, dev)
+        if z is not None:
+            _need(z, "z", u.shape, u.dtype, dev)
+        _need(B, "B", (batch, N, L), u.dtype, dev)
+        _need(C, "C", (batch, N, L), u.dtype, dev)
+        _need(A, "A", (dim, N), torch.float32, dev)
+        for t, name in ((D, "D"), (delta_bias, "delta_bias")):
+            if t is not None:
+                _need(t, name, (dim,), torch.float32, dev)
+        if h0 is not None:
+            _need(h0, "h0", (batch, dim, N), torch.float32, dev)
+        if self.y is None:
+            self.y = torch.empty((batch, dim, L), dtype=out_dtype or torch.float32, device=dev)
+        _need(self.y, "y", (batch, dim, L), None, dev)
+        if self.h_last is not None:
+            _need(self.h_last, "h_last", (batch, dim, N), torch.float32, dev)
+        self._keep = (u, delta, A, B, C, D, delta_bias, z, h0)
+        self._args = ScanArgs(batch, dim, N, L, _dtype_code(u), _dtype_code(self.y), _p(u),
+                              _p(delta), _p(z), _p(A), _p(B), _p(C), _p(D), _p(delta_bias),
+                              int(bool(delta_softplus)), _p(h0), _p(self.y), _p(self.h_last))
+        self.ctx = ctx or default_context(dev.index if dev.index is not None else 0)
+        self._stream = _stream_ptr(stream, dev)
+        self._fn = lib().ss_scan_fwd
+        self._argp = ctypes.byref(self._args)
+
+    def __call__(self):
+        rc = self._fn(self.ctx.handle, self._argp, self._stream)
+        if rc != SS_OK:
+            raise SSError(rc, "ss_scan_fwd")
+        return self.y, self.h_last
+
+
 def ss_state_update(state, x, dt, A, B, C, D=None, dt_bias=None, z=None, dt_softplus=True,
                     y=None, out_dtype=None, ctx: Context | None = None, stream=None):
     """One decode step on the GPU; `state` (batch, dim, N) float32 is updated
@@ -245,5 +294,6 @@ def ss_state_update(state, x, dt, A, B, C, D=None, dt_bias=None, z=None, dt_soft
     return y
 
 
-__all__ = ["ss_scan_fwd", "ss_state_update", "Context", "SSError", "lib", "status_string",
+__all__ = ["ss_scan_fwd", "ss_state_update", "PreparedScan", "Context", "SSError", "lib",
+           "status_string",
            "ScanArgs", "UpdateArgs", "LIB_PATH"]

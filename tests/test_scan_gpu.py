@@ -202,6 +202,23 @@ def test_chained_kernel_needs_whole_tiles():
     _full_check(cfg, ss.SS_VARIANT_AUTO)
 
 
+def test_prepared_call_matches():
+    """A PreparedScan re-enqueues exactly the call ss_scan_fwd makes."""
+    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=2, dim=96, seqlen=256, seed=63)
+    inp = workloads.scan_inputs(cfg, with_h0=True)
+    t = device_inputs(inp, cfg)
+    ctx = _ctx()
+    y0, h0_ = _run(cfg, t, ctx, h0=t["h0"])
+    call = ss.PreparedScan(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"],
+                           delta_bias=t["delta_bias"], z=t["z"], h0=t["h0"],
+                           h_last=torch.empty_like(t["h0"]), ctx=ctx)
+    for _ in range(2):
+        y, hl = call()
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy().astype(np.float64), y0)
+        assert np.array_equal(hl.cpu().numpy().astype(np.float64), h0_)
+
+
 def test_moderate_full_tensor():
     """Every element of a multi-tile, multi-CTA case."""
     cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=2, dim=160, seqlen=1024, seed=55)
