@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the selective scan (S6) and its decode update.
+"""fp64 CPU oracle for the selective scan (S6), its decode update, and the
+causal depthwise convolution of the Mamba block with its decode step.
 
 TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
 CPU-baseline leg are the only callers. The CUDA library never imports it and
@@ -40,6 +41,10 @@ def _load():
         lib.ss_oracle_scan.restype = I
         lib.ss_oracle_state_update.argtypes = [LL, P, P, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I]
         lib.ss_oracle_state_update.restype = I
+        lib.ss_oracle_conv1d.argtypes = [LL, P, I, LL, I, P, P, P, P, I, P, P]
+        lib.ss_oracle_conv1d.restype = I
+        lib.ss_oracle_conv1d_update.argtypes = [LL, P, I, I, P, P, P, I, P, P]
+        lib.ss_oracle_conv1d_update.restype = I
         lib.ss_oracle_softplus.argtypes = [D]
         lib.ss_oracle_softplus.restype = D
         lib.ss_oracle_silu.argtypes = [D]
@@ -154,3 +159,60 @@ def state_update(state, x, dt, A, B, C, D=None, dt_bias=None, z=None, dt_softplu
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return y.reshape(np.asarray(x).shape)
+
+
+def conv1d_fwd(x, weight, bias=None, init_state=None, silu=False, rows=None, dim=None):
+    """Causal depthwise convolution in fp64.
+
+    Full-tensor form: x (batch, dim, L). Row-subset form: x (len(rows), L) with
+    rows (flat indices b*dim+d) and dim. weight (dim, W) float32, bias (dim,)
+    float32 or None; init_state None (zeros) or (rows..., W-1), the W-1 inputs
+    before step 0, oldest first. x is float32 or bf16 bit patterns (uint16).
+    Returns (out, final_state) in float64: out shaped like x, final_state
+    (rows..., W-1), the last W-1 inputs."""
+    x = np.ascontiguousarray(x)
+    weight = np.ascontiguousarray(weight, dtype=np.float32)
+    W = weight.shape[1]
+    if rows is None:
+        batch, dim, L = x.shape
+        rows = np.arange(batch * dim)
+        out_shape, st_shape = x.shape, (batch, dim, W - 1)
+    else:
+        rows = np.asarray(rows, dtype=np.int64)
+        L = x.shape[-1]
+        out_shape, st_shape = (len(rows), L), (len(rows), W - 1)
+    nrows = len(rows)
+    row_d = (rows % dim).astype(np.int32)
+    bp = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    sp = None if init_state is None else \
+        np.ascontiguousarray(init_state, dtype=np.float64).reshape(nrows, W - 1)
+    out = np.empty((nrows, L), dtype=np.float64)
+    fs = np.empty((nrows, max(W - 1, 1)), dtype=np.float64)
+    rc = _load().ss_oracle_conv1d(nrows, _ptr(row_d), W, L, _dtype_code(x), _ptr(x),
+                                  _ptr(weight), _ptr(bp), _ptr(sp), int(bool(silu)), _ptr(out),
+                                  _ptr(fs))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out.reshape(out_shape), fs[:, :W - 1].reshape(st_shape)
+
+
+def conv1d_update(state, x, weight, bias=None, silu=False, dim=None):
+    """One decode step of the convolution in fp64. state (batch, dim, W-1)
+    float64 (oldest input first) is updated in place; x is (batch, dim).
+    Returns out (float64) shaped like x."""
+    x = np.ascontiguousarray(x)
+    weight = np.ascontiguousarray(weight, dtype=np.float32)
+    W = weight.shape[1]
+    dim = x.shape[-1] if dim is None else dim
+    nrows = x.size
+    assert state.dtype == np.float64 and state.flags.c_contiguous and state.size == nrows * (W - 1)
+    rows = np.arange(nrows)
+    row_d = (rows % dim).astype(np.int32)
+    bp = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    out = np.empty(nrows, dtype=np.float64)
+    rc = _load().ss_oracle_conv1d_update(nrows, _ptr(row_d), W, _dtype_code(x), _ptr(x),
+                                         _ptr(weight), _ptr(bp), int(bool(silu)), _ptr(state),
+                                         _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out.reshape(x.shape)

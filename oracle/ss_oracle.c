@@ -179,3 +179,80 @@ int ss_oracle_state_update(long long nrows, const int *row_b, const int *row_d,
     free(h_new);
     return rc;
 }
+
+/*
+ * Causal depthwise 1D convolution of the Mamba block, and its decode step.
+ *
+ * Sources, by page title and section:
+ *  - "Mamba: Linear-Time Sequence Modeling with Selective State Spaces",
+ *    section "Key terms" (Mamba block): the block combines the input
+ *    projection, a 1D convolution, the selective SSM and a multiplicative
+ *    gate.
+ *  - soft186.com, "Mamba选择性状态空间机制", section "基础模型构建": the
+ *    convolution width d_conv = 4, and the install line names the
+ *    causal-conv1d package (the convolution looks only backwards in time).
+ *
+ * Per row (b, d), width W, weights w[d][0..W-1], inputs x[0..L-1]:
+ *   out[l] = bias[d] + sum_{k=0}^{W-1} w[d][k] * xin(l - (W-1) + k)
+ *   xin(j) = x[j] for j >= 0, and the given initial state s[(W-1) + j] for
+ *            -(W-1) <= j < 0 (zero without a state)
+ *   out[l] = silu(out[l]) when asked
+ * The state after the row is its last W-1 inputs, xin(L-(W-1)) .. xin(L-1).
+ */
+static double conv_in(const void *x, long long row_off, long long j, int dtype,
+                      const double *s, int W) {
+    if (j >= 0) return rd(x, row_off + j, dtype);
+    return s ? s[(W - 1) + j] : 0.0;
+}
+
+int ss_oracle_conv1d(long long nrows, const int *row_d, int width, long long seqlen, int dtype,
+                     const void *x, const float *w, const float *bias,
+                     const double *init_state, int silu, double *out, double *final_state) {
+    if (nrows < 0 || width < 1 || seqlen < 0 || !row_d || (seqlen > 0 && (!x || !out)) || !w)
+        return -1;
+    for (long long r = 0; r < nrows; ++r) {
+        const int d = row_d[r];
+        const double *s = init_state ? init_state + r * (width - 1) : NULL;
+        const float *wd = w + (long long)d * width;
+        const long long off = r * seqlen;
+        for (long long l = 0; l < seqlen; ++l) {
+            double acc = bias ? (double)bias[d] : 0.0;
+            for (int k = 0; k < width; ++k)
+                acc += (double)wd[k] * conv_in(x, off, l - (width - 1) + k, dtype, s, width);
+            out[off + l] = silu ? ss_oracle_silu(acc) : acc;
+        }
+        if (final_state) {
+            double *fs = final_state + r * (width - 1);
+            double tmp[64];
+            if (width - 1 > 64) return -1;
+            for (int j = 0; j < width - 1; ++j)
+                tmp[j] = conv_in(x, off, seqlen - (width - 1) + j, dtype, s, width);
+            for (int j = 0; j < width - 1; ++j) fs[j] = tmp[j];
+        }
+    }
+    return 0;
+}
+
+/*
+ * Decode step of the convolution: for each row, out = bias + w[W-1] * x
+ * + sum_{k<W-1} w[k] * state[k] (then silu when asked), and the state drops
+ * its oldest input and appends x. state is (nrows, W-1), oldest first.
+ */
+int ss_oracle_conv1d_update(long long nrows, const int *row_d, int width, int dtype,
+                            const void *x, const float *w, const float *bias, int silu,
+                            double *state, double *out) {
+    if (nrows < 0 || width < 1 || !row_d || !x || !w || !out || (width > 1 && !state)) return -1;
+    for (long long r = 0; r < nrows; ++r) {
+        const int d = row_d[r];
+        const float *wd = w + (long long)d * width;
+        double *s = state + r * (width - 1);
+        const double xv = rd(x, r, dtype);
+        double acc = bias ? (double)bias[d] : 0.0;
+        for (int k = 0; k < width - 1; ++k) acc += (double)wd[k] * s[k];
+        acc += (double)wd[width - 1] * xv;
+        out[r] = silu ? ss_oracle_silu(acc) : acc;
+        for (int k = 0; k + 1 < width - 1; ++k) s[k] = s[k + 1];
+        if (width > 1) s[width - 2] = xv;
+    }
+    return 0;
+}

@@ -278,6 +278,123 @@ def pin_no_softplus(orc, seed=10):
     return max(rel_err(y, y_ref), rel_err(hl, H[..., -1]))
 
 
+# ---------------------------------------------------------------- causal conv1d
+#
+# "Mamba: Linear-Time Sequence Modeling with Selective State Spaces", section
+# "Key terms" (the Mamba block has a 1D convolution in front of the SSM);
+# soft186.com "Mamba选择性状态空间机制", section "基础模型构建" (d_conv = 4, the
+# causal-conv1d package). The reference values come from numpy's own
+# convolution routine, from closed forms and from invariants.
+
+def conv_case(seed, batch=2, dim=3, L=37, W=4, bf16=False, with_bias=True, with_state=False):
+    g = np.random.default_rng(seed)
+    x = g.standard_normal((batch, dim, L)).astype(np.float32)
+    if bf16:
+        x = (x.view(np.uint32) + 0x7FFF + ((x.view(np.uint32) >> 16) & 1)) >> 16
+        x = x.astype(np.uint16)
+    return dict(x=x, weight=g.standard_normal((dim, W)).astype(np.float32),
+                bias=g.standard_normal(dim).astype(np.float32) if with_bias else None,
+                init_state=g.standard_normal((batch, dim, W - 1)) if with_state else None)
+
+
+def _as_f64(x):
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def conv_numpy(c):
+    """out and final state through numpy.convolve on [state, x] ('valid' part)."""
+    x = _as_f64(c["x"])
+    batch, dim, L = x.shape
+    W = c["weight"].shape[1]
+    out = np.empty((batch, dim, L))
+    fs = np.empty((batch, dim, W - 1))
+    for b in range(batch):
+        for d in range(dim):
+            s = c["init_state"][b, d] if c["init_state"] is not None else np.zeros(W - 1)
+            pad = np.concatenate([s, x[b, d]])
+            w = c["weight"][d].astype(np.float64)
+            out[b, d] = np.convolve(pad, w[::-1], mode="valid")
+            if c["bias"] is not None:
+                out[b, d] += c["bias"][d]
+            fs[b, d] = pad[L:L + W - 1]
+    return out, fs
+
+
+def pin_conv_numpy(orc, seed=20):
+    """Widths 2..4, fp32 and bf16 inputs, with and without bias and state."""
+    err = 0.0
+    for W in (2, 3, 4):
+        for bf16 in (False, True):
+            for with_state in (False, True):
+                c = conv_case(seed + W, W=W, bf16=bf16, with_state=with_state,
+                              with_bias=not with_state)
+                out, fs = orc.conv1d_fwd(c["x"], c["weight"], bias=c["bias"],
+                                         init_state=c["init_state"])
+                o_ref, f_ref = conv_numpy(c)
+                err = max(err, rel_err(out, o_ref), rel_err(fs, f_ref))
+    return err
+
+
+def pin_conv_impulse(orc, seed=21, L=12, p=5):
+    """A unit impulse at step p gives bias + w[W-1-(l-p)] for p <= l < p+W, bias elsewhere."""
+    c = conv_case(seed, batch=1, dim=2, L=L)
+    x = np.zeros((1, 2, L), dtype=np.float32)
+    x[0, :, p] = 1.0
+    out, _ = orc.conv1d_fwd(x, c["weight"], bias=c["bias"])
+    W = c["weight"].shape[1]
+    ref = np.tile(c["bias"][None, :, None].astype(np.float64), (1, 1, L))
+    for d in range(2):
+        for l in range(p, min(L, p + W)):
+            ref[0, d, l] += c["weight"][d, W - 1 - (l - p)]
+    return rel_err(out, ref)
+
+
+def pin_conv_short_rows(orc, seed=22):
+    """Rows shorter than the state: the final state keeps part of the initial one."""
+    err = 0.0
+    for L in (1, 2):
+        c = conv_case(seed + L, L=L, with_state=True)
+        out, fs = orc.conv1d_fwd(c["x"], c["weight"], bias=c["bias"], init_state=c["init_state"])
+        o_ref, f_ref = conv_numpy(c)
+        err = max(err, rel_err(out, o_ref), rel_err(fs, f_ref))
+    return err
+
+
+def pin_conv_split(orc, seed=23, L1=9):
+    """[0, L) at once equals [0, L1) then [L1, L) started from the state after L1."""
+    c = conv_case(seed, with_state=True)
+    out, fs = orc.conv1d_fwd(c["x"], c["weight"], bias=c["bias"], init_state=c["init_state"])
+    o1, s1 = orc.conv1d_fwd(np.ascontiguousarray(c["x"][..., :L1]), c["weight"], bias=c["bias"],
+                            init_state=c["init_state"])
+    o2, s2 = orc.conv1d_fwd(np.ascontiguousarray(c["x"][..., L1:]), c["weight"], bias=c["bias"],
+                            init_state=s1)
+    return max(rel_err(np.concatenate([o1, o2], axis=-1), out), rel_err(s2, fs))
+
+
+def pin_conv_decode_chain(orc, seed=24, L=10):
+    """L decode steps equal one forward pass over the same L inputs."""
+    err = 0.0
+    for silu in (False, True):
+        c = conv_case(seed, L=L, with_state=True)
+        out, fs = orc.conv1d_fwd(c["x"], c["weight"], bias=c["bias"], init_state=c["init_state"],
+                                 silu=silu)
+        st = np.ascontiguousarray(c["init_state"], dtype=np.float64).copy()
+        steps = [orc.conv1d_update(st, np.ascontiguousarray(c["x"][..., l]), c["weight"],
+                                   bias=c["bias"], silu=silu) for l in range(L)]
+        err = max(err, rel_err(np.stack(steps, axis=-1), out), rel_err(st, fs))
+    return err
+
+
+def pin_conv_silu(orc, seed=25):
+    """The activation is z * sigmoid(z) of the linear output."""
+    c = conv_case(seed)
+    lin, _ = orc.conv1d_fwd(c["x"], c["weight"], bias=c["bias"])
+    act, _ = orc.conv1d_fwd(c["x"], c["weight"], bias=c["bias"], silu=True)
+    return rel_err(act, silu_ref(lin))
+
+
 ALL_PINS = {
     "materialised": pin_materialised,
     "materialised_h0_noz": lambda o: pin_materialised(o, seed=11, with_h0=True, with_z=False),
@@ -291,6 +408,12 @@ ALL_PINS = {
     "associative_scan": pin_associative_scan,
     "decode_chain": pin_decode_chain,
     "no_softplus": pin_no_softplus,
+    "conv_numpy": pin_conv_numpy,
+    "conv_impulse": pin_conv_impulse,
+    "conv_short_rows": pin_conv_short_rows,
+    "conv_split": pin_conv_split,
+    "conv_decode_chain": pin_conv_decode_chain,
+    "conv_silu": pin_conv_silu,
 }
 
 # every pin must come in under this (fp64 everywhere)

@@ -37,6 +37,21 @@ MUTANTS = {
                  "const double uv = rd(j->u, urow + (l > 0 ? l - 1 : 0), j->dtype);"),
     "z_ignored": ("if (j->z) yv *=", "if (0) yv *="),
     "D_by_n": ("(double)j->D[d]", "(double)j->D[0]"),
+    # causal depthwise convolution and its decode step
+    "conv_kernel_reversed": ("acc += (double)wd[k] * conv_in(x, off, l - (width - 1) + k",
+                             "acc += (double)wd[width - 1 - k] * conv_in(x, off, l - (width - 1) + k"),
+    "conv_not_causal": ("conv_in(x, off, l - (width - 1) + k, dtype, s, width)",
+                        "conv_in(x, off, l - (width - 1) / 2 + k, dtype, s, width)"),
+    "conv_state_ignored": ("return s ? s[(W - 1) + j] : 0.0;", "return 0.0;"),
+    "conv_state_reversed": ("return s ? s[(W - 1) + j] : 0.0;", "return s ? s[-1 - j] : 0.0;"),
+    "conv_bias_dropped": ("double acc = bias ? (double)bias[d] : 0.0;\n            for (int k = 0; k < width; ++k)",
+                          "double acc = 0.0;\n            for (int k = 0; k < width; ++k)"),
+    "conv_final_state_shift": ("seqlen - (width - 1) + j", "seqlen - width + j"),
+    "conv_update_no_shift": ("for (int k = 0; k + 1 < width - 1; ++k) s[k] = s[k + 1];", ";"),
+    "conv_update_weight": ("acc += (double)wd[width - 1] * xv;", "acc += (double)wd[0] * xv;"),
+    "conv_silu_dropped": ("out[off + l] = silu ? ss_oracle_silu(acc) : acc;", "out[off + l] = acc;"),
+    "conv_channel_0": ("const float *wd = w + (long long)d * width;\n        const long long off",
+                       "const float *wd = w;\n        const long long off"),
 }
 
 
@@ -57,7 +72,8 @@ def test_mutant_is_caught(name, tmp_path, monkeypatch):
     oracle._load()
     lib = ctypes.CDLL(_build(name, tmp_path))
     real = oracle._lib
-    for fn in ("ss_oracle_scan", "ss_oracle_state_update", "ss_oracle_softplus", "ss_oracle_silu"):
+    for fn in ("ss_oracle_scan", "ss_oracle_state_update", "ss_oracle_softplus", "ss_oracle_silu",
+               "ss_oracle_conv1d", "ss_oracle_conv1d_update"):
         f = getattr(lib, fn)
         f.argtypes = getattr(real, fn).argtypes
         f.restype = getattr(real, fn).restype
