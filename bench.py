@@ -59,6 +59,7 @@ def parse():
     ap.add_argument("--skip-probe", action="store_true", help="skip the ALU-rate probes")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--skip-decode", action="store_true", help="skip the decode-step leg")
+    ap.add_argument("--skip-conv", action="store_true", help="skip the conv1d leg")
     return ap.parse_args()
 
 
@@ -298,6 +299,49 @@ def time_decode(ss, ctx, dev, stream, args, n_sets=6):
             "steps": steps, "gpu_launches": steps}
 
 
+def time_conv1d(ss, ctx, dev, stream, cfg, args):
+    """Time ss_conv1d_fwd, the Mamba block's causal depthwise convolution
+    (width 4, silu), over the scan workload's (batch, d_inner, L) in its input
+    dtype, output in the same dtype, zero initial state, final state out."""
+    import ctypes
+    import torch
+    W = 4
+    g = torch.Generator(device="cpu").manual_seed(cfg.seed)
+    dt = torch.bfloat16 if cfg.in_dtype == "bf16" else torch.float32
+    x = torch.randn((cfg.batch, cfg.dim, cfg.seqlen), generator=g).to(dt).to(dev)
+    w = torch.randn((cfg.dim, W), generator=g).to(dev)
+    b = torch.randn((cfg.dim,), generator=g).to(dev)
+    out = torch.empty_like(x)
+    fs = torch.empty((cfg.batch, cfg.dim, W - 1), device=dev)
+    a = ss.Conv1dArgs(cfg.batch, cfg.dim, W, cfg.seqlen, 1 if dt == torch.bfloat16 else 0,
+                      1 if dt == torch.bfloat16 else 0, x.data_ptr(), w.data_ptr(),
+                      b.data_ptr(), None, 1, out.data_ptr(), fs.data_ptr())
+    fn, argp = ss.lib().ss_conv1d_fwd, ctypes.byref(a)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    for _ in range(max(args.warmup, 3)):
+        assert fn(ctx.handle, argp, sp) == 0
+    torch.cuda.synchronize(dev)
+    steps = max(args.steps, 1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn(ctx.handle, argp, sp)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    esz = 2 if dt == torch.bfloat16 else 4
+    nbytes = cfg.elements * 2 * esz + cfg.rows * (W - 1) * 4 + cfg.dim * (W + 1) * 4
+    gbs = nbytes / (us * 1e-6) / 1e9
+    peak, src = measured_peaks()
+    return {"workload": "conv1d: batch %d, d_inner %d, L %d, width %d, %s in/out, silu, "
+                        "final state out" % (cfg.batch, cfg.dim, cfg.seqlen, W, cfg.in_dtype),
+            "us_per_call": us, "elements_per_s": cfg.elements / (us * 1e-6),
+            "algorithmic_bytes": nbytes, "gbs": gbs,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "peak_source": src,
+                         "unit": "GB/s", "frac": gbs / peak},
+            "steps": steps, "gpu_launches": steps}
+
+
 def run_ours(args, rank, world, local):
     import torch
     import selective_state_space_136_b300 as ss
@@ -389,6 +433,7 @@ def run_ours(args, rank, world, local):
     host_us_per_call = (t_enq - t_wall0) / args.steps * 1e6
 
     decode = None if args.skip_decode else time_decode(ss, ctx, dev, stream, args)
+    conv1d = None if args.skip_conv else time_conv1d(ss, ctx, dev, stream, cfg, args)
 
     # ---- end to end: pinned host inputs in, y and h_last back to host, every step
     e2e = None
@@ -505,6 +550,7 @@ def run_ours(args, rank, world, local):
         "host_us_per_call": host_us_per_call,
         "alu_probe": probes,
         "decode": decode,
+        "conv1d": conv1d,
         "impl": "ours",
     }
     print(json.dumps(out), flush=True)

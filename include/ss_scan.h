@@ -137,6 +137,62 @@ typedef struct {
 int ss_state_update(ss_ctx *ctx, const ss_update_args *args, ss_stream_t stream);
 
 /*
+ * Causal depthwise 1D convolution: the Mamba block's convolution in front of
+ * the selective scan ("Mamba: Linear-Time Sequence Modeling with Selective
+ * State Spaces", section "Key terms", the Mamba block; soft186.com,
+ * "Mamba选择性状态空间机制", section "基础模型构建": width d_conv = 4 and the
+ * causal-conv1d package). Per row (b, d), W = width:
+ *     out[l] = bias[d] + sum_{k<W} weight[d,k] * xin(l - (W-1) + k)
+ *     xin(j) = x[b,d,j] for j >= 0; init_state[b,d,(W-1)+j] for j < 0
+ *              (zero when init_state is NULL)
+ *     out[l] = silu(out[l])                  when silu != 0
+ *     final_state[b,d,:] = xin(L-(W-1)) .. xin(L-1), the last W-1 inputs
+ *   batch, dim >= 1; width in {2, 3, 4} (else SS_ERR_UNSUPPORTED); seqlen >= 0.
+ *   x     : (batch, dim, seqlen) in in_dtype.   out : same shape, out_dtype;
+ *           must not overlap x.
+ *   weight: (dim, width) fp32.   bias: (dim) fp32 or NULL.
+ *   init_state, final_state: (batch, dim, width-1) fp32, oldest input first,
+ *           or NULL; final_state must not overlap init_state, x or out.
+ *   Device pointers, 16-byte aligned, caller-owned. seqlen == 0 writes
+ *   final_state = init_state (or zeros) and nothing else.
+ */
+typedef struct {
+    int batch, dim, width;
+    long long seqlen;
+    int in_dtype, out_dtype;
+    const void *x;
+    const float *weight, *bias;
+    const float *init_state;
+    int silu;
+    void *out;
+    float *final_state;
+} ss_conv1d_args;
+
+int ss_conv1d_fwd(ss_ctx *ctx, const ss_conv1d_args *args, ss_stream_t stream);
+
+/*
+ * One decode step of the convolution, per row (b, d):
+ *     out = bias[d] + sum_{k<W-1} weight[d,k] * state[b,d,k] + weight[d,W-1] * x[b,d]
+ *     (then silu when silu != 0); state drops its oldest input and appends x.
+ *   state : (batch, dim, width-1) fp32, oldest first, updated in place.
+ *   x, out: (batch, dim) in in_dtype / out_dtype; out must not overlap the
+ *           inputs or the state.
+ * The arithmetic is that of ss_conv1d_fwd with seqlen = 1 and
+ * init_state = final_state = state.
+ */
+typedef struct {
+    int batch, dim, width;
+    int in_dtype, out_dtype;
+    float *state;
+    const void *x;
+    const float *weight, *bias;
+    int silu;
+    void *out;
+} ss_conv1d_update_args;
+
+int ss_conv1d_update(ss_ctx *ctx, const ss_conv1d_update_args *args, ss_stream_t stream);
+
+/*
  * Selective scan forward without any device allocation. The pages have no
  * counterpart to this entry point: it exists for callers that may not call
  * cudaMalloc at all (inside memory-planned or graph-captured regions, in

@@ -44,6 +44,23 @@ class UpdateArgs(ctypes.Structure):
                 ("D", _vp), ("dt_bias", _vp), ("dt_softplus", ctypes.c_int), ("y", _vp)]
 
 
+class Conv1dArgs(ctypes.Structure):
+    """Mirror of ss_conv1d_args."""
+    _fields_ = [("batch", ctypes.c_int), ("dim", ctypes.c_int), ("width", ctypes.c_int),
+                ("seqlen", ctypes.c_longlong), ("in_dtype", ctypes.c_int),
+                ("out_dtype", ctypes.c_int), ("x", _vp), ("weight", _vp), ("bias", _vp),
+                ("init_state", _vp), ("silu", ctypes.c_int), ("out", _vp),
+                ("final_state", _vp)]
+
+
+class Conv1dUpdateArgs(ctypes.Structure):
+    """Mirror of ss_conv1d_update_args."""
+    _fields_ = [("batch", ctypes.c_int), ("dim", ctypes.c_int), ("width", ctypes.c_int),
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("state", _vp),
+                ("x", _vp), ("weight", _vp), ("bias", _vp), ("silu", ctypes.c_int),
+                ("out", _vp)]
+
+
 class SSError(RuntimeError):
     def __init__(self, status, what):
         super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
@@ -67,6 +84,8 @@ def lib():
             L.ss_destroy.argtypes = [_vp]
             L.ss_scan_fwd.argtypes = [_vp, ctypes.POINTER(ScanArgs), _vp]
             L.ss_state_update.argtypes = [_vp, ctypes.POINTER(UpdateArgs), _vp]
+            L.ss_conv1d_fwd.argtypes = [_vp, ctypes.POINTER(Conv1dArgs), _vp]
+            L.ss_conv1d_update.argtypes = [_vp, ctypes.POINTER(Conv1dUpdateArgs), _vp]
             L.ss_get_device_error.argtypes = [_vp, _vp]
             L.ss_status_string.argtypes = [ctypes.c_int]
             L.ss_status_string.restype = ctypes.c_char_p
@@ -294,6 +313,67 @@ def ss_state_update(state, x, dt, A, B, C, D=None, dt_bias=None, z=None, dt_soft
     return y
 
 
-__all__ = ["ss_scan_fwd", "ss_state_update", "PreparedScan", "Context", "SSError", "lib",
-           "status_string",
-           "ScanArgs", "UpdateArgs", "LIB_PATH"]
+def ss_conv1d_fwd(x, weight, bias=None, init_state=None, silu=False, out=None,
+                  final_state=None, out_dtype=None, return_final_state=True,
+                  ctx: Context | None = None, stream=None):
+    """Causal depthwise convolution on the GPU.
+
+    x (batch, dim, L) float32 or bfloat16; weight (dim, W) float32 with W in
+    {2, 3, 4}; bias (dim,) float32 or None; init_state (batch, dim, W-1)
+    float32 or None (the W-1 inputs before step 0, oldest first). out defaults
+    to x's dtype. Returns (out, final_state), final_state (batch, dim, W-1)
+    float32 (None when return_final_state is False and no buffer was given)."""
+    import torch
+    _need(x, "x")
+    batch, dim, L = x.shape
+    dev = x.device
+    _need(weight, "weight", None, torch.float32, dev)
+    if weight.dim() != 2 or weight.shape[0] != dim:
+        raise ValueError("weight must be (dim, width)")
+    W = weight.shape[1]
+    if bias is not None:
+        _need(bias, "bias", (dim,), torch.float32, dev)
+    if init_state is not None:
+        _need(init_state, "init_state", (batch, dim, W - 1), torch.float32, dev)
+    if out is None:
+        out = torch.empty((batch, dim, L), dtype=out_dtype or x.dtype, device=dev)
+    _need(out, "out", (batch, dim, L), None, dev)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, dim, W - 1), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _need(final_state, "final_state", (batch, dim, W - 1), torch.float32, dev)
+    a = Conv1dArgs(batch, dim, W, L, _dtype_code(x), _dtype_code(out), _p(x), _p(weight),
+                   _p(bias), _p(init_state), int(bool(silu)), _p(out), _p(final_state))
+    ctx = ctx or default_context(dev.index if dev.index is not None else 0)
+    _check(lib().ss_conv1d_fwd(ctx.handle, ctypes.byref(a), _stream_ptr(stream, dev)),
+           "ss_conv1d_fwd")
+    return out, final_state
+
+
+def ss_conv1d_update(state, x, weight, bias=None, silu=False, out=None, out_dtype=None,
+                     ctx: Context | None = None, stream=None):
+    """One decode step of the convolution; state (batch, dim, W-1) float32 is
+    updated in place. x (batch, dim). Returns out (batch, dim), x's dtype
+    unless out/out_dtype say otherwise."""
+    import torch
+    _need(state, "state", None, torch.float32)
+    batch, dim, Wm1 = state.shape
+    dev = state.device
+    _need(x, "x", (batch, dim), None, dev)
+    _need(weight, "weight", (dim, Wm1 + 1), torch.float32, dev)
+    if bias is not None:
+        _need(bias, "bias", (dim,), torch.float32, dev)
+    if out is None:
+        out = torch.empty((batch, dim), dtype=out_dtype or x.dtype, device=dev)
+    _need(out, "out", (batch, dim), None, dev)
+    a = Conv1dUpdateArgs(batch, dim, Wm1 + 1, _dtype_code(x), _dtype_code(out), _p(state),
+                         _p(x), _p(weight), _p(bias), int(bool(silu)), _p(out))
+    ctx = ctx or default_context(dev.index if dev.index is not None else 0)
+    _check(lib().ss_conv1d_update(ctx.handle, ctypes.byref(a), _stream_ptr(stream, dev)),
+           "ss_conv1d_update")
+    return out
+
+
+__all__ = ["ss_scan_fwd", "ss_state_update", "ss_conv1d_fwd", "ss_conv1d_update",
+           "PreparedScan", "Context", "SSError", "lib", "status_string",
+           "ScanArgs", "UpdateArgs", "Conv1dArgs", "Conv1dUpdateArgs", "LIB_PATH"]

@@ -327,4 +327,77 @@ int ss_state_update(ss_ctx *ctx, const ss_update_args *a, ss_stream_t stream) {
     return rc;
 }
 
+int ss_conv1d_fwd(ss_ctx *ctx, const ss_conv1d_args *a, ss_stream_t stream) {
+    if (!ctx || !a) return SS_ERR_INVALID_ARG;
+    if (a->batch < 1 || a->dim < 1 || a->seqlen < 0) return SS_ERR_INVALID_ARG;
+    if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return SS_ERR_INVALID_ARG;
+    if (a->width < 2 || a->width > 4) return SS_ERR_UNSUPPORTED;
+    if ((long long)a->batch * a->dim > (1LL << 40) || a->seqlen >= (1LL << 40))
+        return SS_ERR_INVALID_ARG;
+    if (!a->weight || (a->seqlen > 0 && (!a->x || !a->out))) return SS_ERR_INVALID_ARG;
+    const void *ptrs[] = {a->x, a->weight, a->bias, a->init_state, a->out, a->final_state};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return SS_ERR_INVALID_ARG;
+    const size_t rows = (size_t)a->batch * a->dim;
+    const size_t n = rows * (size_t)a->seqlen;
+    const size_t esz = a->in_dtype == SS_BF16 ? 2 : 4, osz = a->out_dtype == SS_BF16 ? 2 : 4;
+    const size_t st_b = rows * (size_t)(a->width - 1) * 4;
+    const Span x = span(a->x, n * esz), out = span(a->out, n * osz);
+    const Span init = span(a->init_state, a->init_state ? st_b : 0);
+    const Span fin = span(a->final_state, a->final_state ? st_b : 0);
+    const Span params[] = {span(a->weight, (size_t)a->dim * a->width * 4),
+                           span(a->bias, a->bias ? (size_t)a->dim * 4 : 0)};
+    if (overlaps(out, x) || overlaps(out, init)) return SS_ERR_INVALID_ARG;
+    if (overlaps(fin, init) || overlaps(fin, x) || overlaps(fin, out)) return SS_ERR_INVALID_ARG;
+    for (const Span &s : params)
+        if (overlaps(out, s) || overlaps(fin, s)) return SS_ERR_INVALID_ARG;
+    if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    ctx->last_variant = 0;
+    if (a->seqlen == 0) {
+        ctx->last_launches = 0;
+        if (!a->final_state) return SS_OK;
+        const cudaError_t e = a->init_state
+                                  ? cudaMemcpyAsync(a->final_state, a->init_state, st_b,
+                                                    cudaMemcpyDeviceToDevice, st)
+                                  : cudaMemsetAsync(a->final_state, 0, st_b, st);
+        return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    }
+    ssh::ConvParams p{a->batch, a->dim, a->width, a->seqlen, a->in_dtype, a->out_dtype, a->x,
+                      a->weight, a->bias, a->init_state, a->silu, a->out, a->final_state};
+    const int rc = ssh::launch_conv1d(p, st);
+    ctx->last_launches = rc == SS_OK ? 1 : 0;
+    return rc;
+}
+
+int ss_conv1d_update(ss_ctx *ctx, const ss_conv1d_update_args *a, ss_stream_t stream) {
+    if (!ctx || !a) return SS_ERR_INVALID_ARG;
+    if (a->batch < 1 || a->dim < 1) return SS_ERR_INVALID_ARG;
+    if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return SS_ERR_INVALID_ARG;
+    if (a->width < 2 || a->width > 4) return SS_ERR_UNSUPPORTED;
+    if ((long long)a->batch * a->dim > (1LL << 40)) return SS_ERR_INVALID_ARG;
+    if (!a->state || !a->x || !a->weight || !a->out) return SS_ERR_INVALID_ARG;
+    const void *ptrs[] = {a->state, a->x, a->weight, a->bias, a->out};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return SS_ERR_INVALID_ARG;
+    const size_t rows = (size_t)a->batch * a->dim;
+    const size_t esz = a->in_dtype == SS_BF16 ? 2 : 4, osz = a->out_dtype == SS_BF16 ? 2 : 4;
+    const Span out = span(a->out, rows * osz);
+    const Span stt = span(a->state, rows * (size_t)(a->width - 1) * 4);
+    const Span ins[] = {stt, span(a->x, rows * esz),
+                        span(a->weight, (size_t)a->dim * a->width * 4),
+                        span(a->bias, a->bias ? (size_t)a->dim * 4 : 0)};
+    for (const Span &s : ins)
+        if (overlaps(out, s)) return SS_ERR_INVALID_ARG;
+    for (size_t i = 1; i < sizeof(ins) / sizeof(ins[0]); ++i)
+        if (overlaps(stt, ins[i])) return SS_ERR_INVALID_ARG;
+    if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
+    ssh::ConvUpdateParams p{a->batch, a->dim, a->width, a->in_dtype, a->out_dtype, a->state,
+                            a->x, a->weight, a->bias, a->silu, a->out};
+    const int rc = ssh::launch_conv1d_update(p, reinterpret_cast<cudaStream_t>(stream));
+    ctx->last_variant = 0;
+    ctx->last_launches = rc == SS_OK ? 1 : 0;
+    return rc;
+}
+
 }  // extern "C"

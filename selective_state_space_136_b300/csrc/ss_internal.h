@@ -90,4 +90,27 @@ struct UpdateParams {
 };
 int launch_update(const UpdateParams &p, cudaStream_t st);
 
+// causal depthwise conv1d (ss_conv.cu)
+struct ConvParams {
+    int batch, dim, width;
+    long long seqlen;
+    int in_dtype, out_dtype;
+    const void *x;
+    const float *w, *bias, *init_state;
+    int silu;
+    void *out;
+    float *final_state;
+};
+int launch_conv1d(const ConvParams &p, cudaStream_t st);
+struct ConvUpdateParams {
+    int batch, dim, width;
+    int in_dtype, out_dtype;
+    float *state;
+    const void *x;
+    const float *w, *bias;
+    int silu;
+    void *out;
+};
+int launch_conv1d_update(const ConvUpdateParams &p, cudaStream_t st);
+
 }  // namespace ssh

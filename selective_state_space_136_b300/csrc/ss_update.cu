@@ -91,7 +91,9 @@ __global__ void __launch_bounds__(256) state_update_kernel(const ssh::UpdatePara
     const bool ok = row_raw < rows;
     // threads past the end keep running on row 0 so the shuffles stay full-warp
     const long long row = ok ? row_raw : 0;
-    const int b = (int)(row / p.dim), d = (int)(row % p.dim);
+    // 32-bit division (the launcher keeps batch * dim * TPR below 2^31)
+    const uint32_t bq = (uint32_t)row / (uint32_t)p.dim;
+    const int b = (int)bq, d = (int)((uint32_t)row - bq * (uint32_t)p.dim);
 
     float st[NS], A[NS], Bv[NS], Cv[NS];
     ld_f32<NS>(p.state + row * N + q * NS, st);
@@ -123,6 +125,7 @@ __global__ void __launch_bounds__(256) state_update_kernel(const ssh::UpdatePara
 template <typename Tin, typename Tout>
 int launch_n(const ssh::UpdateParams &p, cudaStream_t st) {
     const long long rows = (long long)p.batch * p.dim;
+    if (rows * 16 >= (1LL << 31)) return SS_ERR_UNSUPPORTED;
     auto go = [&](auto kern, int tpr) {
         const long long threads = rows * tpr;
         kern<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(p);

@@ -34,29 +34,30 @@ def test_every_declared_symbol_is_exported(built):
 def test_struct_layout_matches_binding(built, tmp_path):
     """ctypes mirrors of the argument structs have the C layout."""
     import selective_state_space_136_b300 as ss
+    structs = {"ss_scan_args": ss.ScanArgs, "ss_update_args": ss.UpdateArgs,
+               "ss_conv1d_args": ss.Conv1dArgs, "ss_conv1d_update_args": ss.Conv1dUpdateArgs}
     prog = tmp_path / "layout.c"
-    fields_scan = [f for f, _ in ss.ScanArgs._fields_]
-    fields_upd = [f for f, _ in ss.UpdateArgs._fields_]
-    body = ['#include <stdio.h>', '#include <stddef.h>', '#include "ss_scan.h"', "int main(void){",
-            'printf("%zu %zu\\n", sizeof(ss_scan_args), sizeof(ss_update_args));']
-    for f in fields_scan:
-        body.append('printf("S %s %%zu\\n", offsetof(ss_scan_args, %s));' % (f, f))
-    for f in fields_upd:
-        body.append('printf("U %s %%zu\\n", offsetof(ss_update_args, %s));' % (f, f))
+    body = ['#include <stdio.h>', '#include <stddef.h>', '#include "ss_scan.h"', "int main(void){"]
+    for cname, cls in structs.items():
+        body.append('printf("%s size %%zu\\n", sizeof(%s));' % (cname, cname))
+        for f, _ in cls._fields_:
+            body.append('printf("%s %s %%zu\\n", offsetof(%s, %s));' % (cname, f, cname, f))
     body.append("return 0;}")
     prog.write_text("\n".join(body))
     exe = tmp_path / "layout"
     subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(prog)])
-    out = subprocess.check_output([str(exe)]).decode().split("\n")
-    s_size, u_size = map(int, out[0].split())
-    assert s_size == ctypes.sizeof(ss.ScanArgs)
-    assert u_size == ctypes.sizeof(ss.UpdateArgs)
-    for line in out[1:]:
+    seen = set()
+    for line in subprocess.check_output([str(exe)]).decode().split("\n"):
         if not line:
             continue
-        kind, name, off = line.split()
-        cls = ss.ScanArgs if kind == "S" else ss.UpdateArgs
-        assert getattr(cls, name).offset == int(off), (kind, name)
+        cname, name, val = line.split()
+        cls = structs[cname]
+        if name == "size":
+            assert int(val) == ctypes.sizeof(cls), cname
+        else:
+            assert getattr(cls, name).offset == int(val), (cname, name)
+        seen.add(cname)
+    assert seen == set(structs)
 
 
 def test_host_validation_without_gpu(built):
@@ -64,6 +65,8 @@ def test_host_validation_without_gpu(built):
     L = ss.lib()
     assert L.ss_scan_fwd(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_state_update(None, None, None) == ss.SS_ERR_INVALID_ARG
+    assert L.ss_conv1d_fwd(None, None, None) == ss.SS_ERR_INVALID_ARG
+    assert L.ss_conv1d_update(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_set_option(None, 0, 0) == ss.SS_ERR_INVALID_ARG
     assert L.ss_destroy(None) == ss.SS_OK
     assert ss.status_string(ss.SS_ERR_TIMEOUT) == "device wait timed out"
