@@ -37,9 +37,11 @@ def _load():
     if _lib is None:
         lib = ctypes.CDLL(build())
         P, I, LL, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_double
-        lib.ss_oracle_scan.argtypes = [LL, P, P, I, I, LL, I, P, P, P, P, P, P, P, P, I, P, P, P, I]
+        lib.ss_oracle_scan.argtypes = [LL, P, P, I, I, LL, I, P, P, P, P, P, P, P, P, I, P, P, P, I,
+                                       I]
         lib.ss_oracle_scan.restype = I
-        lib.ss_oracle_state_update.argtypes = [LL, P, P, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I]
+        lib.ss_oracle_state_update.argtypes = [LL, P, P, I, I, I, P, P, P, P, P, P, P, P, P, I, P,
+                                               I, I]
         lib.ss_oracle_state_update.restype = I
         lib.ss_oracle_conv1d.argtypes = [LL, P, I, LL, I, P, P, P, P, I, P, P]
         lib.ss_oracle_conv1d.restype = I
@@ -81,7 +83,7 @@ def silu(x: float) -> float:
 
 
 def scan_fwd(u, delta, A, B, C, D=None, delta_bias=None, z=None, delta_softplus=True,
-             h0=None, rows=None, dim=None, threads=None):
+             h0=None, rows=None, dim=None, threads=None, zoh=False):
     """Selective scan forward in fp64.
 
     Full-tensor form: u, delta, z of shape (batch, dim, L); B, C (batch, N, L).
@@ -90,6 +92,8 @@ def scan_fwd(u, delta, A, B, C, D=None, delta_bias=None, z=None, delta_softplus=
     A is (dim, N) float32; D and delta_bias (dim,) float32 or None.
     Inputs are float32, or uint16 bf16 bit patterns (all of one kind).
     h0: None (zero state) or (rows..., N).
+    zoh: use the exact zero-order-hold input matrix (exp(dt A) - 1) / A * B
+    instead of dt * B.
     Returns (y, h_last) in float64, shaped like u and (rows..., N)."""
     u = np.ascontiguousarray(u)
     full = rows is None
@@ -122,7 +126,7 @@ def scan_fwd(u, delta, A, B, C, D=None, delta_bias=None, z=None, delta_softplus=
     rc = _load().ss_oracle_scan(nrows, _ptr(row_b), _ptr(row_d), dim, N, L, code, _ptr(u2),
                                 _ptr(d2), _ptr(z2), _ptr(A), _ptr(B), _ptr(C), _ptr(Dp),
                                 _ptr(bp), int(bool(delta_softplus)), _ptr(h0p), _ptr(y), _ptr(hl),
-                                threads or _cpu_threads())
+                                int(bool(zoh)), threads or _cpu_threads())
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     if full:
@@ -131,7 +135,7 @@ def scan_fwd(u, delta, A, B, C, D=None, delta_bias=None, z=None, delta_softplus=
 
 
 def state_update(state, x, dt, A, B, C, D=None, dt_bias=None, z=None, dt_softplus=True,
-                 rows=None, dim=None, threads=None):
+                 rows=None, dim=None, threads=None, zoh=False):
     """One decode step in fp64. state (batch, dim, N) float64 is updated in
     place; x, dt, z are (batch, dim) (or (len(rows),) with rows/dim given);
     B, C are (batch, N). Returns y (float64) shaped like x."""
@@ -155,7 +159,8 @@ def state_update(state, x, dt, A, B, C, D=None, dt_bias=None, z=None, dt_softplu
     rc = _load().ss_oracle_state_update(nrows, _ptr(row_b), _ptr(row_d), dim, N, code,
                                         _ptr(state), _ptr(x), _ptr(dt), _ptr(z), _ptr(A),
                                         _ptr(B), _ptr(C), _ptr(Dp), _ptr(bp),
-                                        int(bool(dt_softplus)), _ptr(y), threads or 1)
+                                        int(bool(dt_softplus)), _ptr(y), int(bool(zoh)),
+                                        threads or 1)
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return y.reshape(np.asarray(x).shape)

@@ -71,6 +71,7 @@ typedef struct {
     const void *B, *C;                 /* (batch, dstate, seqlen) */
     const float *D, *bias;             /* (dim); may be NULL */
     int softplus;
+    int zoh;                           /* 1: exact zero-order-hold input matrix */
     const double *h0;                  /* (nrows, dstate) or NULL */
     /* outputs */
     double *y;                         /* (nrows, seqlen) or NULL */
@@ -78,6 +79,18 @@ typedef struct {
     /* work split */
     long long lo, hi;
 } scan_job;
+
+/*
+ * The factor that turns B into the discrete input matrix, per state:
+ *  - simplified (soft186.com article, "动态参数化的状态空间"): dt;
+ *  - exact zero-order hold ("Mamba: Linear-Time Sequence Modeling with
+ *    Selective State Spaces", section "Method": B_bar = (dt A)^-1 (exp(dt A) - I) dt B,
+ *    diagonal A): (exp(dt a) - 1) / a, whose limit at a = 0 is dt.
+ */
+static double input_factor(double dt, double a, int zoh) {
+    if (!zoh || a == 0.0) return dt;
+    return expm1(dt * a) / a;
+}
 
 static void scan_rows(const scan_job *j) {
     const long long L = j->seqlen;
@@ -99,7 +112,8 @@ static void scan_rows(const scan_job *j) {
                 const double a = (double)j->A[(long long)d * N + n];
                 const double Bv = rd(j->B, bcrow + (long long)n * L + l, j->dtype);
                 const double Cv = rd(j->C, bcrow + (long long)n * L + l, j->dtype);
-                h[n] = exp(dt * a) * h[n] + dt * Bv * uv;
+                const double bbar = input_factor(dt, a, j->zoh);
+                h[n] = exp(dt * a) * h[n] + bbar * Bv * uv;
                 yv += Cv * h[n];
             }
             yv += Dd * uv;
@@ -132,14 +146,14 @@ int ss_oracle_scan(long long nrows, const int *row_b, const int *row_d, int dim,
                    const void *delta, const void *z, const float *A, const void *B,
                    const void *C, const float *D, const float *delta_bias,
                    int delta_softplus, const double *h0, double *y, double *h_last,
-                   int nthreads) {
+                   int zoh, int nthreads) {
     if (nrows < 0 || dim <= 0 || dstate <= 0 || seqlen < 0) return -1;
     if (!row_b || !row_d || !u || !delta || !A || !B || !C) return -1;
     if (dtype != ORC_F32 && dtype != ORC_BF16) return -1;
     for (long long r = 0; r < nrows; ++r)
         if (row_d[r] < 0 || row_d[r] >= dim || row_b[r] < 0) return -1;
     scan_job base = {nrows, seqlen, dim, dstate, dtype, row_b, row_d, u, delta, z,
-                     A, B, C, D, delta_bias, delta_softplus, h0, y, h_last, 0, nrows};
+                     A, B, C, D, delta_bias, delta_softplus, zoh, h0, y, h_last, 0, nrows};
     if (nthreads <= 1 || nrows < 2) {
         scan_rows(&base);
         return 0;
@@ -170,11 +184,11 @@ int ss_oracle_state_update(long long nrows, const int *row_b, const int *row_d,
                            const void *x, const void *dt, const void *z,
                            const float *A, const void *B, const void *C,
                            const float *D, const float *dt_bias, int dt_softplus,
-                           double *y, int nthreads) {
+                           double *y, int zoh, int nthreads) {
     if (!state) return -1;
     double *h_new = (double *)malloc(sizeof(double) * (size_t)(nrows * dstate + 1));
     int rc = ss_oracle_scan(nrows, row_b, row_d, dim, dstate, 1, dtype, x, dt, z, A,
-                            B, C, D, dt_bias, dt_softplus, state, y, h_new, nthreads);
+                            B, C, D, dt_bias, dt_softplus, state, y, h_new, zoh, nthreads);
     if (rc == 0) memcpy(state, h_new, sizeof(double) * (size_t)(nrows * dstate));
     free(h_new);
     return rc;

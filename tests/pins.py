@@ -278,6 +278,70 @@ def pin_no_softplus(orc, seed=10):
     return max(rel_err(y, y_ref), rel_err(hl, H[..., -1]))
 
 
+# ---------------------------------------------------------------- exact zero-order hold
+#
+# "Mamba: Linear-Time Sequence Modeling with Selective State Spaces", section
+# "Method": B_bar = (dt A)^-1 (exp(dt A) - I) dt B. For diagonal A the factor
+# per state is (exp(dt a) - 1) / a; section "The Selection Mechanism (S6)":
+# with N = 1, A = -1, B = 1 this makes the recurrence exactly the gated RNN
+# h_t = (1 - g_t) h_{t-1} + g_t x_t with g_t = sigmoid(delta_t).
+
+def pin_zoh_gated_rnn(orc, seed=30, L=50):
+    """N = 1, A = -1, B = C = 1, D = 0, no gate, exact ZOH: h_t = (1 - g) h + g u."""
+    g = np.random.default_rng(seed)
+    u = g.standard_normal((1, 1, L)).astype(np.float32)
+    delta = g.standard_normal((1, 1, L)).astype(np.float32)
+    ones = np.ones((1, 1, L), dtype=np.float32)
+    A = -np.ones((1, 1), dtype=np.float32)
+    y, hl = orc.scan_fwd(u, delta, A, ones, ones, D=None, delta_bias=None, z=None, zoh=True)
+    gate = 1.0 / (1.0 + np.exp(-delta[0, 0].astype(np.float64)))
+    h = 0.0
+    href = np.empty(L)
+    for t in range(L):
+        h = (1.0 - gate[t]) * h + gate[t] * float(u[0, 0, t])
+        href[t] = h
+    return max(rel_err(y[0, 0], href), rel_err(hl[0, 0, 0], href[-1]))
+
+
+def pin_zoh_lti(orc, seed=31, dim=2, N=3, L=48):
+    """Constant dt, B, C: y = K * u + D u with K_i = sum_n C_n dA_n^i (dA_n - 1)/A_n B_n."""
+    g = np.random.default_rng(seed)
+    u = g.standard_normal((1, dim, L)).astype(np.float32)
+    dconst = g.standard_normal(dim).astype(np.float32)
+    delta = np.repeat(dconst[None, :, None], L, axis=2).astype(np.float32)
+    Bn = g.standard_normal(N).astype(np.float32)
+    Cn = g.standard_normal(N).astype(np.float32)
+    B = np.repeat(Bn[None, :, None], L, axis=2).astype(np.float32)
+    C = np.repeat(Cn[None, :, None], L, axis=2).astype(np.float32)
+    A = -(g.uniform(0.1, 3.0, (dim, N))).astype(np.float32)
+    D = g.standard_normal(dim).astype(np.float32)
+    y, _ = orc.scan_fwd(u, delta, A, B, C, D=D, delta_bias=None, z=None, zoh=True)
+    err = 0.0
+    for d in range(dim):
+        dt = float(softplus_ref(np.float64(dconst[d])))
+        a = A[d].astype(np.float64)
+        dA = np.exp(dt * a)
+        bbar = (dA - 1.0) / a * Bn.astype(np.float64)
+        i = np.arange(L)
+        K = (Cn.astype(np.float64)[None, :] * dA[None, :] ** i[:, None] * bbar[None, :]).sum(axis=1)
+        uu = u[0, d].astype(np.float64)
+        err = max(err, rel_err(y[0, d], np.convolve(uu, K)[:L] + float(D[d]) * uu))
+    return err
+
+
+def pin_zoh_decode_chain(orc, seed=32, k=10):
+    """Chained single-token ZOH updates equal one ZOH scan from the same h0."""
+    c = small_case(seed=seed, with_h0=True, L=k)
+    y, hl = orc.scan_fwd(c["u"], c["delta"], c["A"], c["B"], c["C"], D=c["D"],
+                         delta_bias=c["delta_bias"], z=c["z"], h0=c["h0"], zoh=True)
+    state = np.ascontiguousarray(c["h0"].astype(np.float64))
+    ys = [orc.state_update(state, c["u"][..., t].copy(), c["delta"][..., t].copy(), c["A"],
+                           c["B"][..., t].copy(), c["C"][..., t].copy(), D=c["D"],
+                           dt_bias=c["delta_bias"], z=c["z"][..., t].copy(), zoh=True)
+          for t in range(k)]
+    return max(rel_err(np.stack(ys, axis=-1), y), rel_err(state, hl))
+
+
 # ---------------------------------------------------------------- causal conv1d
 #
 # "Mamba: Linear-Time Sequence Modeling with Selective State Spaces", section
@@ -408,6 +472,9 @@ ALL_PINS = {
     "associative_scan": pin_associative_scan,
     "decode_chain": pin_decode_chain,
     "no_softplus": pin_no_softplus,
+    "zoh_gated_rnn": pin_zoh_gated_rnn,
+    "zoh_lti": pin_zoh_lti,
+    "zoh_decode_chain": pin_zoh_decode_chain,
     "conv_numpy": pin_conv_numpy,
     "conv_impulse": pin_conv_impulse,
     "conv_short_rows": pin_conv_short_rows,

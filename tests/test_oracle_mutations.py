@@ -18,7 +18,7 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "ss_oracle.c")
 
 MUTANTS = {
     "exp_sign": ("exp(dt * a)", "exp(-dt * a)"),
-    "drop_dt_in_input": ("dt * Bv * uv", "Bv * uv"),
+    "drop_dt_in_input": ("bbar * Bv * uv", "Bv * uv"),
     "B_transposed": ("rd(j->B, bcrow + (long long)n * L + l", "rd(j->B, bcrow + l * N + n"),
     "C_reads_B": ("rd(j->C, bcrow", "rd(j->B, bcrow"),
     "drop_D_skip": ("yv += Dd * uv;", ";"),
@@ -28,8 +28,8 @@ MUTANTS = {
     "softplus_sign": ("x + log1p(exp(-x))", "x + log1p(exp(x))"),
     "ignore_h0": ("h[n] = j->h0 ? j->h0[r * N + n] : 0.0;", "h[n] = 0.0;"),
     "output_before_update": (
-        "h[n] = exp(dt * a) * h[n] + dt * Bv * uv;\n                yv += Cv * h[n];",
-        "yv += Cv * h[n];\n                h[n] = exp(dt * a) * h[n] + dt * Bv * uv;"),
+        "h[n] = exp(dt * a) * h[n] + bbar * Bv * uv;\n                yv += Cv * h[n];",
+        "yv += Cv * h[n];\n                h[n] = exp(dt * a) * h[n] + bbar * Bv * uv;"),
     "sigmoid_not_silu": ("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
     "bias_by_batch": ("j->bias[d]", "j->bias[b % j->dim]"),
     "A_transposed": ("j->A[(long long)d * N + n]", "j->A[(long long)n * j->dim + d]"),
@@ -37,6 +37,10 @@ MUTANTS = {
                  "const double uv = rd(j->u, urow + (l > 0 ? l - 1 : 0), j->dtype);"),
     "z_ignored": ("if (j->z) yv *=", "if (0) yv *="),
     "D_by_n": ("(double)j->D[d]", "(double)j->D[0]"),
+    # exact zero-order hold
+    "zoh_ignored": ("if (!zoh || a == 0.0) return dt;", "return dt;"),
+    "zoh_sign": ("return expm1(dt * a) / a;", "return expm1(-dt * a) / a;"),
+    "zoh_no_division": ("return expm1(dt * a) / a;", "return -expm1(dt * a);"),
     # causal depthwise convolution and its decode step
     "conv_kernel_reversed": ("acc += (double)wd[k] * conv_in(x, off, l - (width - 1) + k",
                              "acc += (double)wd[width - 1 - k] * conv_in(x, off, l - (width - 1) + k"),
