@@ -255,6 +255,16 @@ const char *ss_status_string(int status);
  *   SS_OPT_WAIT_LIMIT       polls before a device-side wait gives up and
  *                           reports SS_ERR_TIMEOUT (default 2^22, roughly a
  *                           second; 1 .. 2^30).
+ *   SS_OPT_DISCRETIZATION   input matrix of ss_scan_fwd and ss_state_update:
+ *                           SS_DISC_SIMPLIFIED (default) uses dt * B, the step
+ *                           the soft186.com article prints ("动态参数化的状态空间");
+ *                           SS_DISC_ZOH uses the exact zero-order hold
+ *                           (exp(dt A) - 1) / A * B of the Mamba page's section
+ *                           "Method" (dt * B where A = 0). ZOH runs on the
+ *                           one-thread-per-row kernels only: AUTO picks them,
+ *                           and forcing the pair, split-row or chunked kernels
+ *                           returns SS_ERR_UNSUPPORTED. ss_scan_fwd_noalloc
+ *                           always uses the simplified form.
  *   SS_OPT_TEST_DROP_TILE   test hook: the rows kernel never issues the loads
  *                           of this tile index, so its wait runs out and the
  *                           timeout path is exercised (-1 = off, the default).
@@ -273,8 +283,11 @@ typedef enum {
     SS_OPT_THREADS_PER_ROW = 2,
     SS_OPT_WAIT_LIMIT = 3,
     SS_OPT_TEST_DROP_TILE = 4,
-    SS_OPT_RESIDENT_WARPS = 5
+    SS_OPT_RESIDENT_WARPS = 5,
+    SS_OPT_DISCRETIZATION = 6
 } ss_option;
+
+typedef enum { SS_DISC_SIMPLIFIED = 0, SS_DISC_ZOH = 1 } ss_discretization;
 
 int ss_set_option(ss_ctx *ctx, int option, long long value);
 

@@ -136,6 +136,10 @@ int ss_set_option(ss_ctx *ctx, int option, long long value) {
             if (value < 0 || value > 64) return SS_ERR_INVALID_ARG;
             ctx->warps_per_sm = (int)value;
             return SS_OK;
+        case SS_OPT_DISCRETIZATION:
+            if (value != SS_DISC_SIMPLIFIED && value != SS_DISC_ZOH) return SS_ERR_INVALID_ARG;
+            ctx->zoh = (int)value;
+            return SS_OK;
         case SS_OPT_WAIT_LIMIT:
             if (value < 1 || value > (1LL << 30)) return SS_ERR_INVALID_ARG;
             ctx->wait_limit = (uint32_t)value;
@@ -229,10 +233,11 @@ int ss_scan_fwd(ss_ctx *ctx, const ss_scan_args *a, ss_stream_t stream) {
     ssh::ScanParams p{a->batch, a->dim, a->dstate, a->seqlen, a->in_dtype, a->out_dtype,
                       a->u, a->delta, a->z, a->A, a->B, a->C, a->D, a->delta_bias,
                       a->delta_softplus, a->h0, a->y, a->h_last, ctx->d_err, ctx->wait_limit,
-                      ctx->drop_tile};
+                      ctx->drop_tile, ctx->zoh};
     int variant = ctx->variant;
     const bool rows_ok = ssh::rows_supported(p) && ssh::seq_supported(p);
-    const bool pair_ok = ssh::pair_supported(p);
+    // the exact zero-order hold runs on the one-thread-per-row kernels only
+    const bool pair_ok = ssh::pair_supported(p) && !ctx->zoh;
     const long long resident = (long long)(ctx->warps_per_sm > 0 ? ctx->warps_per_sm : 8) *
                                ctx->sm_count;
     if (variant == SS_VARIANT_AUTO) {
@@ -265,9 +270,10 @@ int ss_scan_fwd(ss_ctx *ctx, const ss_scan_args *a, ss_stream_t stream) {
         launches = n_seg >= 2 ? 4 : 2;
     } else if (variant == SS_VARIANT_ROWS) {
         int tpr = ctx->rows_tpr;
-        if (tpr == 0) tpr = ssh::pair_supported(p) ? 2 : 1;
+        if (tpr == 0) tpr = pair_ok ? 2 : 1;
+        if (ctx->zoh && tpr != 1) return SS_ERR_UNSUPPORTED;
         if (tpr == 2) {
-            if (!ssh::pair_supported(p)) return SS_ERR_UNSUPPORTED;
+            if (!pair_ok) return SS_ERR_UNSUPPORTED;
             ssh::PairWork w{};
             const int n_seg = 1;  // the chained kernel balances by tile ranges, not segments
             if ((rc = ensure_pair_scratch(ctx, p, n_seg, false, &w)) != SS_OK) return rc;
@@ -320,7 +326,7 @@ int ss_state_update(ss_ctx *ctx, const ss_update_args *a, ss_stream_t stream) {
     if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
     ssh::UpdateParams p{a->batch, a->dim, a->dstate, a->in_dtype, a->out_dtype, a->state,
                         a->x, a->dt, a->z, a->A, a->B, a->C, a->D, a->dt_bias,
-                        a->dt_softplus, a->y};
+                        a->dt_softplus, a->y, ctx->zoh};
     const int rc = ssh::launch_update(p, reinterpret_cast<cudaStream_t>(stream));
     ctx->last_variant = 0;
     ctx->last_launches = rc == SS_OK ? 1 : 0;

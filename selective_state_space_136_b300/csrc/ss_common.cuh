@@ -15,6 +15,7 @@
 namespace ssk {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // ---------------------------------------------------------------- element io
 // Inputs arrive as fp32 or as bf16 bit patterns; both widen exactly to fp32.
@@ -45,6 +46,16 @@ __device__ __forceinline__ float softplus(float x) {
 // silu(z) = z * sigmoid(z) = z / (1 + e^-z). For z << 0 the denominator
 // overflows to +inf and the quotient is -0, the right limit.
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + ex2(-z * kLog2e)); }
+
+// Exact zero-order hold for one state ("Mamba: Linear-Time Sequence Modeling
+// with Selective State Spaces", section "Method", diagonal A): the decay
+// e = exp(dt a) and the input factor (exp(dt a) - 1) / a (dt at a = 0), with
+// exp(dt a) - 1 from expm1f so that small dt a keeps its precision.
+__device__ __forceinline__ float zoh_step(float dt, float a, float *e) {
+    const float em1 = expm1f(dt * a);
+    *e = 1.f + em1;
+    return a != 0.f ? em1 / a : dt;
+}
 
 // Packed fp32x2 arithmetic (two lanes per instruction on sm_100+).
 struct f2 {

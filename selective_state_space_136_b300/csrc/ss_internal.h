@@ -22,6 +22,7 @@ struct ss_ctx {
     unsigned long long epoch = 0;  // calls that used the chained scratch
     uint32_t wait_limit = 1u << 22;  // polls before a device wait gives up
     int drop_tile = -1;            // test hook: a tile whose loads are never issued
+    int zoh = 0;                   // SS_DISC_ZOH: exact zero-order-hold input matrix
     int last_variant = 0;
     int last_launches = 0;
 };
@@ -44,6 +45,7 @@ struct ScanParams {
     int *err;
     uint32_t wait_limit;
     int drop_tile;
+    int zoh;  // exact zero-order-hold input matrix (one-thread-per-row kernels only)
 };
 
 int launch_simple(const ScanParams &p, cudaStream_t st);
@@ -87,6 +89,7 @@ struct UpdateParams {
     const float *D, *bias;
     int softplus;
     void *y;
+    int zoh;
 };
 int launch_update(const UpdateParams &p, cudaStream_t st);
 

@@ -107,7 +107,7 @@ extern "C" int ss_scan_fwd_noalloc(const ss_scan_args *a, int *device_error,
     ssh::ScanParams p{a->batch, a->dim, a->dstate, a->seqlen, a->in_dtype, a->out_dtype,
                       a->u, a->delta, a->z, a->A, a->B, a->C, a->D, a->delta_bias,
                       a->delta_softplus, a->h0, a->y, a->h_last, device_error,
-                      1u << 22, -1};
+                      1u << 22, -1, 0};
     // this entry point serves the chained pair-row kernel only
     if (!ssh::pair_supported(p)) return SS_ERR_UNSUPPORTED;
     size_t flags_b = 0, carry_b = 0;

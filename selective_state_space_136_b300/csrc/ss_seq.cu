@@ -104,7 +104,22 @@ __device__ __forceinline__ f2 pair_at(const uint32_t *w, int i, float) {
 // One recurrence step for all N states of a row; returns sum_n C_n h_n.
 template <int N>
 __device__ __forceinline__ float step_states(f2 *h, const f2 *A2, float dt, float du,
-                                             const float *Bl, const float *Cl) {
+                                             const float *Bl, const float *Cl, float uv,
+                                             bool zoh) {
+    if (zoh) {
+        // exact zero-order hold, one state at a time (A2 holds A log2(e))
+        float acc = 0.f;
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            float &hn = (n & 1) ? h[n / 2].y : h[n / 2].x;
+            const float a = ((n & 1) ? A2[n / 2].y : A2[n / 2].x) * kLn2;
+            float e;
+            const float f = zoh_step(dt, a, &e);
+            hn = fmaf(e, hn, f * uv * Bl[n]);
+            acc = fmaf(Cl[n], hn, acc);
+        }
+        return acc;
+    }
     if constexpr (N == 1) {
         const float e = ex2(dt * A2[0].x);
         h[0].x = fmaf(e, h[0].x, du * Bl[0]);
@@ -309,11 +324,12 @@ __global__ void __launch_bounds__(32 * W, SS_SEQ_MINB)
         float out[TL];
 #pragma unroll
         for (int i = 0; i < TL / 2; ++i) {
+            const f2 uo = pair_at(uw, i, Tin());
             out[2 * i] = step_states<N>(h, A2, dt[i].x, du[i].x, fB + (2 * i) * LY::FSTRIDE,
-                                        fC + (2 * i) * LY::FSTRIDE);
+                                        fC + (2 * i) * LY::FSTRIDE, uo.x, p.zoh);
             out[2 * i + 1] = step_states<N>(h, A2, dt[i].y, du[i].y,
                                             fB + (2 * i + 1) * LY::FSTRIDE,
-                                            fC + (2 * i + 1) * LY::FSTRIDE);
+                                            fC + (2 * i + 1) * LY::FSTRIDE, uo.y, p.zoh);
         }
         // phase 3: D skip and silu(z) gate
 #pragma unroll

@@ -43,8 +43,15 @@ __global__ void __launch_bounds__(128) scan_simple_kernel(const ssh::ScanParams 
         float acc = 0.f;
 #pragma unroll
         for (int n = 0; n < N; ++n) {
-            const float e = ex2(dt * A2[n]);
-            h[n] = fmaf(e, h[n], dtu * to_f32(Bm[(long long)n * L + l]));
+            const float Bv = to_f32(Bm[(long long)n * L + l]);
+            if (p.zoh) {
+                float e;
+                const float f = zoh_step(dt, p.A[(long long)d * N + n], &e);
+                h[n] = fmaf(e, h[n], f * uv * Bv);
+            } else {
+                const float e = ex2(dt * A2[n]);
+                h[n] = fmaf(e, h[n], dtu * Bv);
+            }
             acc = fmaf(to_f32(Cm[(long long)n * L + l]), h[n], acc);
         }
         acc = fmaf(Dd, uv, acc);

@@ -107,8 +107,14 @@ __global__ void __launch_bounds__(256) state_update_kernel(const ssh::UpdatePara
     float acc = 0.f;
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
-        const float e = ex2(dt * (A[i] * kLog2e));
-        st[i] = fmaf(e, st[i], dtx * Bv[i]);
+        if (p.zoh) {
+            float e;
+            const float f = zoh_step(dt, A[i], &e);
+            st[i] = fmaf(e, st[i], f * xv * Bv[i]);
+        } else {
+            const float e = ex2(dt * (A[i] * kLog2e));
+            st[i] = fmaf(e, st[i], dtx * Bv[i]);
+        }
         acc = fmaf(Cv[i], st[i], acc);
     }
 #pragma unroll

@@ -368,3 +368,41 @@ def test_device_wait_times_out_cleanly(tpr, drop):
     y, hl = _run(cfg, t, ctx)
     y_ref, _ = oracle_rows(inp, cfg, np.arange(cfg.rows))
     check_close(y.reshape(cfg.rows, -1), y_ref, True, "after timeout")
+
+
+# ---------------------------------------------------------------- exact zero-order hold
+
+@pytest.mark.parametrize("N,L,dt", [(16, 256, "bf16"), (16, 100, "f32"), (4, 64, "f32"),
+                                    (16, 2048, "bf16")])
+def test_zoh_scan(N, L, dt):
+    """SS_DISC_ZOH: the input matrix (exp(dt A) - 1) / A * B, against the oracle's ZOH."""
+    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=2, dim=64, dstate=N, seqlen=L,
+                           in_dtype=dt, seed=90 + N + L)
+    inp = workloads.scan_inputs(cfg, with_h0=True)
+    t = device_inputs(inp, cfg)
+    ctx = _ctx()
+    ctx.set_option(ss.SS_OPT_DISCRETIZATION, ss.SS_DISC_ZOH)
+    y, hl = _run(cfg, t, ctx, h0=t["h0"])
+    assert ctx.last_launch()[0] in (ss.SS_VARIANT_ROWS, ss.SS_VARIANT_SIMPLE)
+    rows = np.arange(cfg.rows)
+    A = inp["A"]
+    y_ref, h_ref = oracle.scan_fwd(inp["u"], inp["delta"], A, inp["B"], inp["C"], D=inp["D"],
+                                   delta_bias=inp["delta_bias"], z=inp["z"], h0=inp["h0"],
+                                   rows=rows, dim=cfg.dim, zoh=True)
+    check_close(y.reshape(cfg.rows, -1), y_ref, dt == "bf16", "y")
+    check_close(hl.reshape(cfg.rows, -1), h_ref, dt == "bf16", "h_last")
+    # and it is not the simplified result
+    y_s, _ = oracle_rows(inp, cfg, rows, h0=inp["h0"])
+    assert np.max(np.abs(y_s - y_ref)) > 1e-3 * np.max(np.abs(y_ref))
+
+
+def test_zoh_forced_fast_kernels_unsupported():
+    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=1, dim=64, seqlen=256, seed=95)
+    inp = workloads.scan_inputs(cfg)
+    t = device_inputs(inp, cfg)
+    for variant, tpr in ((ss.SS_VARIANT_ROWS, 2), (ss.SS_VARIANT_ROWS, 4), (ss.SS_VARIANT_CHUNKED, 0)):
+        ctx = _ctx(variant, tpr)
+        ctx.set_option(ss.SS_OPT_DISCRETIZATION, ss.SS_DISC_ZOH)
+        with pytest.raises(ss.SSError) as ei:
+            _run(cfg, t, ctx)
+        assert ei.value.status == ss.SS_ERR_UNSUPPORTED

@@ -97,3 +97,28 @@ def test_decode_config_1000_chained_steps():
         worst = max(worst, check_close(yv, y_ref, True, "decode y step %d" % step))
     sv = st_dev.reshape(-1, cfg.dstate)[rows_t].cpu().numpy()
     check_close(sv, ref_state, True, "decode state after %d steps" % cfg.steps)
+
+
+@pytest.mark.parametrize("N", [4, 16])
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_update_zoh(N, dt):
+    """SS_DISC_ZOH decode steps against the oracle's exact zero-order hold."""
+    cfg = workloads.DecodeConfig("small", 3, 37, N, dt, 70 + N, 5, 1e-3, 1e-1)
+    par = workloads.params(cfg)
+    state = workloads.decode_state0(cfg)
+    st_dev = torch.from_numpy(state).cuda()
+    ref_state = state.astype(np.float64).copy()
+    A, D, bias = (torch.from_numpy(par[k]).cuda() for k in ("A", "D", "delta_bias"))
+    ctx = ss.Context(0)
+    ctx.set_option(ss.SS_OPT_DISCRETIZATION, ss.SS_DISC_ZOH)
+    for step in range(cfg.steps):
+        s = workloads.decode_step_inputs(cfg, step)
+        t = _step_tensors(s)
+        y = ss.ss_state_update(st_dev, t["x"], t["dt"], A, t["B"], t["C"], D=D, dt_bias=bias,
+                               z=t["z"], ctx=ctx)
+        y_ref = oracle.state_update(ref_state, s["x"], s["dt"], par["A"], s["B"], s["C"],
+                                    D=par["D"], dt_bias=par["delta_bias"], z=s["z"], zoh=True)
+        torch.cuda.synchronize()
+        bf = dt == "bf16"
+        check_close(y.cpu().numpy(), y_ref, bf, "y step %d" % step)
+        check_close(st_dev.cpu().numpy(), ref_state, bf, "state step %d" % step)
