@@ -43,6 +43,9 @@ def _load():
         lib.ss_oracle_state_update.argtypes = [LL, P, P, I, I, I, P, P, P, P, P, P, P, P, P, I, P,
                                                I, I]
         lib.ss_oracle_state_update.restype = I
+        lib.ss_oracle_scan_bwd.argtypes = [LL, P, P, I, I, LL, I, P, P, P, P, P, P, P, P, I, P, I,
+                                           P, P, P, P, P, P, P, P, P, P, P]
+        lib.ss_oracle_scan_bwd.restype = I
         lib.ss_oracle_conv1d.argtypes = [LL, P, I, LL, I, P, P, P, P, I, P, P]
         lib.ss_oracle_conv1d.restype = I
         lib.ss_oracle_conv1d_update.argtypes = [LL, P, I, I, P, P, P, I, P, P]
@@ -221,3 +224,43 @@ def conv1d_update(state, x, weight, bias=None, silu=False, dim=None):
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return out.reshape(x.shape)
+
+
+def scan_bwd(u, delta, A, B, C, dy, D=None, delta_bias=None, z=None, delta_softplus=True,
+             h0=None, dh_last=None, zoh=False):
+    """Gradients of the selective scan in fp64 (full tensors only).
+
+    Same inputs as scan_fwd plus dy (batch, dim, L) and optional dh_last
+    (batch, dim, N). Returns a dict with du, ddelta, dz (None without z), dA,
+    dB, dC, dD, ddelta_bias and dh0, all float64."""
+    u = np.ascontiguousarray(u)
+    batch, dim, L = u.shape
+    B = np.ascontiguousarray(B)
+    C = np.ascontiguousarray(C)
+    N = B.shape[1]
+    nrows = batch * dim
+    rows = np.arange(nrows)
+    row_b = (rows // dim).astype(np.int32)
+    row_d = (rows % dim).astype(np.int32)
+    code = _dtype_code(u)
+    cont = lambda a: None if a is None else np.ascontiguousarray(a)
+    delta, z = cont(delta), cont(z)
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    Dp = None if D is None else np.ascontiguousarray(D, dtype=np.float32)
+    bp = None if delta_bias is None else np.ascontiguousarray(delta_bias, dtype=np.float32)
+    h0p = None if h0 is None else np.ascontiguousarray(h0, dtype=np.float64)
+    dyp = np.ascontiguousarray(dy, dtype=np.float64)
+    dhp = None if dh_last is None else np.ascontiguousarray(dh_last, dtype=np.float64)
+    out = dict(du=np.zeros((batch, dim, L)), ddelta=np.zeros((batch, dim, L)),
+               dz=np.zeros((batch, dim, L)) if z is not None else None,
+               dA=np.zeros((dim, N)), dB=np.zeros((batch, N, L)), dC=np.zeros((batch, N, L)),
+               dD=np.zeros(dim), ddelta_bias=np.zeros(dim), dh0=np.zeros((batch, dim, N)))
+    rc = _load().ss_oracle_scan_bwd(
+        nrows, _ptr(row_b), _ptr(row_d), dim, N, L, code, _ptr(u), _ptr(delta), _ptr(z),
+        _ptr(A), _ptr(B), _ptr(C), _ptr(Dp), _ptr(bp), int(bool(delta_softplus)), _ptr(h0p),
+        int(bool(zoh)), _ptr(dyp), _ptr(dhp), _ptr(out["du"]), _ptr(out["ddelta"]),
+        _ptr(out["dz"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+        _ptr(out["ddelta_bias"]), _ptr(out["dh0"]))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out

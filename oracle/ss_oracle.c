@@ -270,3 +270,108 @@ int ss_oracle_conv1d_update(long long nrows, const int *row_d, int width, int dt
     }
     return 0;
 }
+
+/*
+ * Backward pass of the selective scan: the gradients of a scalar loss with
+ * respect to every input, given dy = dL/dy and optionally dh_last = dL/dh_L.
+ * This is reverse-mode differentiation of the forward recurrence above, row
+ * by row, in fp64; the forward states of a row are recomputed and kept in full
+ * (this oracle has no memory limit). With x = delta + bias, dt = softplus(x),
+ * e_n = exp(dt a_n), s = sum_n C_n h_n + D u, y = s silu(z):
+ *   gs   = dy silu(z)                     gz = dy s silu'(z)
+ *   g_n  = dL/dh_n(t) = gs C_n + e_n(t+1) g_n(t+1)   (+ dh_last at t = L-1)
+ *   dC_n += gs h_n(t)          dB_n += g_n f_n u      (f_n: dt, or the ZOH factor)
+ *   du   += gs D + sum_n g_n f_n B_n                  dD += gs u
+ *   ddt   = sum_n g_n (a_n e_n h_n(t-1) + df_n/ddt B_n u)
+ *   dA_n += g_n (dt e_n h_n(t-1) + df_n/da_n B_n u)
+ *   ddelta = ddt sigmoid(x) (softplus) or ddt;  dbias += ddelta
+ *   dh0_n = e_n(0) g_n(0)
+ * dA, dB, dC, dD and dbias are sums over rows and must be zeroed by the
+ * caller; the per-row outputs are overwritten.
+ */
+int ss_oracle_scan_bwd(long long nrows, const int *row_b, const int *row_d, int dim,
+                       int dstate, long long seqlen, int dtype, const void *u,
+                       const void *delta, const void *z, const float *A, const void *B,
+                       const void *C, const float *D, const float *delta_bias,
+                       int delta_softplus, const double *h0, int zoh, const double *dy,
+                       const double *dh_last, double *du, double *ddelta, double *dz,
+                       double *dA, double *dB, double *dC, double *dD, double *dbias,
+                       double *dh0) {
+    if (nrows < 0 || dim <= 0 || dstate <= 0 || seqlen < 0) return -1;
+    if (!row_b || !row_d || !u || !delta || !A || !B || !C || !dy) return -1;
+    const long long L = seqlen;
+    const int N = dstate;
+    double *H = (double *)malloc(sizeof(double) * (size_t)((L + 1) * N + 1));  /* h(-1..L-1) */
+    double *g = (double *)malloc(sizeof(double) * (size_t)N);
+    for (long long r = 0; r < nrows; ++r) {
+        const int b = row_b[r], d = row_d[r];
+        const long long urow = r * L;
+        const long long bcrow = (long long)b * N * L;
+        const double bias = delta_bias ? (double)delta_bias[d] : 0.0;
+        const double Dd = D ? (double)D[d] : 0.0;
+        /* forward, keeping every state: H[(t+1)*N + n] = h_n(t), H[n] = h_n(-1) */
+        for (int n = 0; n < N; ++n) H[n] = h0 ? h0[r * N + n] : 0.0;
+        for (long long t = 0; t < L; ++t) {
+            const double uv = rd(u, urow + t, dtype);
+            const double x = rd(delta, urow + t, dtype) + bias;
+            const double dt = delta_softplus ? ss_oracle_softplus(x) : x;
+            for (int n = 0; n < N; ++n) {
+                const double a = (double)A[(long long)d * N + n];
+                const double Bv = rd(B, bcrow + (long long)n * L + t, dtype);
+                H[(t + 1) * N + n] = exp(dt * a) * H[t * N + n] + input_factor(dt, a, zoh) * Bv * uv;
+            }
+        }
+        /* reverse */
+        for (int n = 0; n < N; ++n) g[n] = dh_last ? dh_last[r * N + n] : 0.0;
+        double gD = 0.0, gbias = 0.0;
+        for (long long t = L - 1; t >= 0; --t) {
+            const double uv = rd(u, urow + t, dtype);
+            const double x = rd(delta, urow + t, dtype) + bias;
+            const double dt = delta_softplus ? ss_oracle_softplus(x) : x;
+            double s = Dd * uv;
+            for (int n = 0; n < N; ++n)
+                s += rd(C, bcrow + (long long)n * L + t, dtype) * H[(t + 1) * N + n];
+            double gs = dy[urow + t];
+            if (z) {
+                const double zv = rd(z, urow + t, dtype);
+                const double sg = 1.0 / (1.0 + exp(-zv));
+                if (dz) dz[urow + t] = dy[urow + t] * s * sg * (1.0 + zv * (1.0 - sg));
+                gs = dy[urow + t] * zv * sg;
+            }
+            gD += gs * uv;
+            double gu = gs * Dd, gdt = 0.0;
+            for (int n = 0; n < N; ++n) {
+                const double a = (double)A[(long long)d * N + n];
+                const double Bv = rd(B, bcrow + (long long)n * L + t, dtype);
+                const double Cv = rd(C, bcrow + (long long)n * L + t, dtype);
+                const double e = exp(dt * a);
+                const double hp = H[t * N + n];
+                g[n] += gs * Cv;
+                if (dC) dC[bcrow + (long long)n * L + t] += gs * H[(t + 1) * N + n];
+                const double f = input_factor(dt, a, zoh);
+                /* derivatives of the input factor f(dt, a) */
+                double fdt = 1.0, fa = 0.0;
+                if (zoh && a != 0.0) {
+                    fdt = e;                                  /* d/ddt (e^{dt a}-1)/a */
+                    fa = (dt * e) / a - expm1(dt * a) / (a * a);
+                }
+                if (dB) dB[bcrow + (long long)n * L + t] += g[n] * f * uv;
+                gu += g[n] * f * Bv;
+                gdt += g[n] * (a * e * hp + fdt * Bv * uv);
+                if (dA) dA[(long long)d * N + n] += g[n] * (dt * e * hp + fa * Bv * uv);
+                g[n] *= e;
+            }
+            const double gx = delta_softplus ? gdt / (1.0 + exp(-x)) : gdt;
+            if (du) du[urow + t] = gu;
+            if (ddelta) ddelta[urow + t] = gx;
+            gbias += gx;
+        }
+        if (dD) dD[d] += gD;
+        if (dbias) dbias[d] += gbias;
+        if (dh0)
+            for (int n = 0; n < N; ++n) dh0[r * N + n] = g[n];
+    }
+    free(H);
+    free(g);
+    return 0;
+}

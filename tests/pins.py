@@ -342,6 +342,59 @@ def pin_zoh_decode_chain(orc, seed=32, k=10):
     return max(rel_err(np.stack(ys, axis=-1), y), rel_err(state, hl))
 
 
+# ---------------------------------------------------------------- backward pass
+#
+# The gradients are pinned to the (pinned) forward pass by central finite
+# differences of the loss sum(dy * y) + sum(dh_last * h_last): every input is
+# perturbed one element at a time. fp32 inputs move by a power of two so the
+# perturbed values are exact; the forward runs in fp64.
+
+def _fd_case(seed, zoh=False, softplus=True):
+    g = np.random.default_rng(seed)
+    batch, dim, N, L = 2, 2, 3, 6
+    f = lambda *s: g.standard_normal(s).astype(np.float32)
+    c = dict(u=f(batch, dim, L), delta=f(batch, dim, L), z=f(batch, dim, L),
+             A=-(g.uniform(0.3, 2.0, (dim, N))).astype(np.float32), B=f(batch, N, L),
+             C=f(batch, N, L), D=f(dim), delta_bias=(g.uniform(-2.0, 0.5, dim)).astype(np.float32),
+             h0=g.standard_normal((batch, dim, N)))
+    if not softplus:
+        c["delta"] = (np.abs(c["delta"]) * 0.3).astype(np.float32)
+        c["delta_bias"] = (np.abs(c["delta_bias"]) * 0.1).astype(np.float32)
+    dy = g.standard_normal((batch, dim, L))
+    dh = g.standard_normal((batch, dim, N))
+    return c, dy, dh
+
+
+def _loss(orc, c, dy, dh, zoh, softplus):
+    y, hl = orc.scan_fwd(c["u"], c["delta"], c["A"], c["B"], c["C"], D=c["D"],
+                         delta_bias=c["delta_bias"], z=c["z"], delta_softplus=softplus, h0=c["h0"],
+                         zoh=zoh)
+    return float(np.sum(dy * y) + np.sum(dh * hl))
+
+
+def pin_bwd_finite_diff(orc, seed=40, zoh=False, softplus=True):
+    c, dy, dh = _fd_case(seed, zoh, softplus)
+    grads = orc.scan_bwd(c["u"], c["delta"], c["A"], c["B"], c["C"], dy, D=c["D"],
+                         delta_bias=c["delta_bias"], z=c["z"], delta_softplus=softplus, h0=c["h0"],
+                         dh_last=dh, zoh=zoh)
+    names = {"u": "du", "delta": "ddelta", "z": "dz", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "delta_bias": "ddelta_bias", "h0": "dh0"}
+    err = 0.0
+    for k, gk in names.items():
+        base = c[k]
+        eps = 1e-6 if base.dtype == np.float64 else 2.0 ** -14
+        fd = np.empty(base.shape)
+        for idx in np.ndindex(base.shape):
+            plus, minus = base.copy(), base.copy()
+            plus[idx] += eps
+            minus[idx] -= eps
+            lp = _loss(orc, {**c, k: plus}, dy, dh, zoh, softplus)
+            lm = _loss(orc, {**c, k: minus}, dy, dh, zoh, softplus)
+            fd[idx] = (lp - lm) / (float(plus[idx]) - float(minus[idx]))
+        err = max(err, rel_err(grads[gk], fd))
+    return err
+
+
 # ---------------------------------------------------------------- causal conv1d
 #
 # "Mamba: Linear-Time Sequence Modeling with Selective State Spaces", section
@@ -475,6 +528,9 @@ ALL_PINS = {
     "zoh_gated_rnn": pin_zoh_gated_rnn,
     "zoh_lti": pin_zoh_lti,
     "zoh_decode_chain": pin_zoh_decode_chain,
+    "bwd_finite_diff": pin_bwd_finite_diff,
+    "bwd_finite_diff_zoh": lambda o: pin_bwd_finite_diff(o, seed=41, zoh=True),
+    "bwd_finite_diff_no_softplus": lambda o: pin_bwd_finite_diff(o, seed=42, softplus=False),
     "conv_numpy": pin_conv_numpy,
     "conv_impulse": pin_conv_impulse,
     "conv_short_rows": pin_conv_short_rows,
@@ -484,5 +540,6 @@ ALL_PINS = {
 }
 
 # every pin must come in under this (fp64 everywhere)
-PIN_TOL = {"small_delta": 1e-9}
+PIN_TOL = {"small_delta": 1e-9, "bwd_finite_diff": 1e-6, "bwd_finite_diff_zoh": 1e-6,
+           "bwd_finite_diff_no_softplus": 1e-6}
 DEFAULT_TOL = 1e-11

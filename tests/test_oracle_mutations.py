@@ -17,7 +17,8 @@ import pins
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ss_oracle.c")
 
 MUTANTS = {
-    "exp_sign": ("exp(dt * a)", "exp(-dt * a)"),
+    "exp_sign": ("h[n] = exp(dt * a) * h[n]", "h[n] = exp(-dt * a) * h[n]"),
+    "bwd_recompute_exp_sign": ("H[(t + 1) * N + n] = exp(dt * a) *", "H[(t + 1) * N + n] = exp(-dt * a) *"),
     "drop_dt_in_input": ("bbar * Bv * uv", "Bv * uv"),
     "B_transposed": ("rd(j->B, bcrow + (long long)n * L + l", "rd(j->B, bcrow + l * N + n"),
     "C_reads_B": ("rd(j->C, bcrow", "rd(j->B, bcrow"),
@@ -41,6 +42,17 @@ MUTANTS = {
     "zoh_ignored": ("if (!zoh || a == 0.0) return dt;", "return dt;"),
     "zoh_sign": ("return expm1(dt * a) / a;", "return expm1(-dt * a) / a;"),
     "zoh_no_division": ("return expm1(dt * a) / a;", "return -expm1(dt * a);"),
+    # backward pass
+    "bwd_no_decay_propagation": ("g[n] *= e;", ";"),
+    "bwd_dC_prev_state": ("+= gs * H[(t + 1) * N + n];", "+= gs * H[t * N + n];"),
+    "bwd_gdt_no_input_term": ("gdt += g[n] * (a * e * hp + fdt * Bv * uv);",
+                              "gdt += g[n] * (a * e * hp);"),
+    "bwd_dz_sigmoid_only": ("dy[urow + t] * s * sg * (1.0 + zv * (1.0 - sg))", "dy[urow + t] * s * sg"),
+    "bwd_zoh_fa_dropped": ("(dt * e * hp + fa * Bv * uv)", "(dt * e * hp)"),
+    "bwd_gx_no_sigmoid": ("const double gx = delta_softplus ? gdt / (1.0 + exp(-x)) : gdt;",
+                          "const double gx = gdt;"),
+    "bwd_dh_last_ignored": ("g[n] = dh_last ? dh_last[r * N + n] : 0.0;", "g[n] = 0.0;"),
+    "bwd_gu_no_D": ("double gu = gs * Dd, gdt = 0.0;", "double gu = 0.0, gdt = 0.0;"),
     # causal depthwise convolution and its decode step
     "conv_kernel_reversed": ("acc += (double)wd[k] * conv_in(x, off, l - (width - 1) + k",
                              "acc += (double)wd[width - 1 - k] * conv_in(x, off, l - (width - 1) + k"),
@@ -77,7 +89,7 @@ def test_mutant_is_caught(name, tmp_path, monkeypatch):
     lib = ctypes.CDLL(_build(name, tmp_path))
     real = oracle._lib
     for fn in ("ss_oracle_scan", "ss_oracle_state_update", "ss_oracle_softplus", "ss_oracle_silu",
-               "ss_oracle_conv1d", "ss_oracle_conv1d_update"):
+               "ss_oracle_conv1d", "ss_oracle_conv1d_update", "ss_oracle_scan_bwd"):
         f = getattr(lib, fn)
         f.argtypes = getattr(real, fn).argtypes
         f.restype = getattr(real, fn).restype
