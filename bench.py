@@ -60,6 +60,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--skip-decode", action="store_true", help="skip the decode-step leg")
     ap.add_argument("--skip-conv", action="store_true", help="skip the conv1d leg")
+    ap.add_argument("--skip-bwd", action="store_true", help="skip the backward leg")
     return ap.parse_args()
 
 
@@ -342,6 +343,53 @@ def time_conv1d(ss, ctx, dev, stream, cfg, args):
             "steps": steps, "gpu_launches": steps}
 
 
+def time_bwd(ss, ctx, dev, stream, cfg, d, params, args):
+    """Time ss_scan_bwd on the scan workload (the forward inputs already on the
+    device, dy fp32, all gradients requested)."""
+    import ctypes
+    import torch
+    L, N = cfg.seqlen, cfg.dstate
+    dy = torch.randn((cfg.batch, cfg.dim, L), device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = [torch.empty((cfg.batch, cfg.dim, L), **f32) for _ in range(3)]
+    gA = torch.empty((cfg.dim, N), **f32)
+    gB, gC = (torch.empty((cfg.batch, N, L), **f32) for _ in range(2))
+    gD, gb = (torch.empty((cfg.dim,), **f32) for _ in range(2))
+    a = ss.ScanBwdArgs(cfg.batch, cfg.dim, N, L, 1 if cfg.in_dtype == "bf16" else 0,
+                       d["u"].data_ptr(), d["delta"].data_ptr(), d["z"].data_ptr(),
+                       params["A"].data_ptr(), d["B"].data_ptr(), d["C"].data_ptr(),
+                       params["D"].data_ptr(), params["delta_bias"].data_ptr(), 1, None,
+                       dy.data_ptr(), None, g[0].data_ptr(), g[1].data_ptr(), g[2].data_ptr(),
+                       gA.data_ptr(), gB.data_ptr(), gC.data_ptr(), gD.data_ptr(), gb.data_ptr(),
+                       None)
+    fn, argp = ss.lib().ss_scan_bwd, ctypes.byref(a)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    for _ in range(2):
+        assert fn(ctx.handle, argp, sp) == 0
+    torch.cuda.synchronize(dev)
+    steps = max(1, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn(ctx.handle, argp, sp)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ctx.device_error() != ss.SS_OK:
+        raise RuntimeError("device error in the backward leg")
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    esz = 2 if cfg.in_dtype == "bf16" else 4
+    # read u, delta, z, dy and B, C; write du, ddelta, dz, dB, dC (fp32)
+    nbytes = cfg.elements * (3 * esz + 4 + 3 * 4) + cfg.batch * N * L * (2 * esz + 2 * 4)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    peak, src = measured_peaks()
+    return {"workload": "scan backward: batch %d, d_inner %d, d_state %d, L %d, %s inputs, fp32 "
+                        "dy and gradients, all gradients" % (cfg.batch, cfg.dim, N, L,
+                                                            cfg.in_dtype),
+            "us_per_call": us, "elements_per_s": cfg.elements / (us * 1e-6),
+            "algorithmic_bytes": nbytes, "gbs": gbs, "hbm_frac": gbs / peak,
+            "hbm_peak_source": src, "steps": steps, "gpu_launches": steps}
+
+
 def run_ours(args, rank, world, local):
     import torch
     import selective_state_space_136_b300 as ss
@@ -434,6 +482,7 @@ def run_ours(args, rank, world, local):
 
     decode = None if args.skip_decode else time_decode(ss, ctx, dev, stream, args)
     conv1d = None if args.skip_conv else time_conv1d(ss, ctx, dev, stream, cfg, args)
+    bwd = None if args.skip_bwd else time_bwd(ss, ctx, dev, stream, cfg, d, params, args)
 
     # ---- end to end: pinned host inputs in, y and h_last back to host, every step
     e2e = None
@@ -551,6 +600,7 @@ def run_ours(args, rank, world, local):
         "alu_probe": probes,
         "decode": decode,
         "conv1d": conv1d,
+        "backward": bwd,
         "impl": "ours",
     }
     print(json.dumps(out), flush=True)

@@ -137,6 +137,45 @@ typedef struct {
 int ss_state_update(ss_ctx *ctx, const ss_update_args *args, ss_stream_t stream);
 
 /*
+ * Backward pass of the selective scan: the gradients of a loss with respect to
+ * every input of ss_scan_fwd, given dy = dL/dy and optionally dh_last =
+ * dL/dh_L. The forward states are recomputed, not stored ("Mamba: Linear-Time
+ * Sequence Modeling with Selective State Spaces", section "Hardware-aware
+ * state expansion": recomputation in the backward pass); the context keeps a
+ * checkpoint of every row's state every 16 steps (batch * ceil(dim/32) * 32 *
+ * seqlen/16 * dstate floats of scratch, allocated on first need).
+ *   Inputs as for ss_scan_fwd (same shapes, in_dtype for u, delta, z, B, C).
+ *   dy     : (batch, dim, seqlen) fp32.   dh_last: (batch, dim, dstate) fp32 or NULL.
+ *   Outputs, fp32, overwritten:
+ *     du, ddelta : (batch, dim, seqlen);  dz: same, or NULL (skipped; must be
+ *                  NULL when z is NULL)
+ *     dA         : (dim, dstate);  dB, dC: (batch, dstate, seqlen)
+ *     dD, ddelta_bias : (dim) or NULL;  dh0: (batch, dim, dstate) or NULL
+ *   seqlen must be a multiple of 16 and the discretization SS_DISC_SIMPLIFIED,
+ *   else SS_ERR_UNSUPPORTED. Outputs must not overlap inputs or each other.
+ *   dB and dC are sums over channels accumulated with atomic adds, so their
+ *   low bits may differ from run to run.
+ */
+typedef struct {
+    int batch, dim, dstate;
+    long long seqlen;
+    int in_dtype;
+    const void *u, *delta, *z;
+    const float *A;
+    const void *B, *C;
+    const float *D, *delta_bias;
+    int delta_softplus;
+    const float *h0;
+    const float *dy, *dh_last;
+    float *du, *ddelta, *dz;
+    float *dA, *dB, *dC;
+    float *dD, *ddelta_bias;
+    float *dh0;
+} ss_scan_bwd_args;
+
+int ss_scan_bwd(ss_ctx *ctx, const ss_scan_bwd_args *args, ss_stream_t stream);
+
+/*
  * Causal depthwise 1D convolution: the Mamba block's convolution in front of
  * the selective scan ("Mamba: Linear-Time Sequence Modeling with Selective
  * State Spaces", section "Key terms", the Mamba block; soft186.com,

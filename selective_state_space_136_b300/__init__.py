@@ -45,6 +45,16 @@ class UpdateArgs(ctypes.Structure):
                 ("D", _vp), ("dt_bias", _vp), ("dt_softplus", ctypes.c_int), ("y", _vp)]
 
 
+class ScanBwdArgs(ctypes.Structure):
+    """Mirror of ss_scan_bwd_args."""
+    _fields_ = [("batch", ctypes.c_int), ("dim", ctypes.c_int), ("dstate", ctypes.c_int),
+                ("seqlen", ctypes.c_longlong), ("in_dtype", ctypes.c_int), ("u", _vp),
+                ("delta", _vp), ("z", _vp), ("A", _vp), ("B", _vp), ("C", _vp), ("D", _vp),
+                ("delta_bias", _vp), ("delta_softplus", ctypes.c_int), ("h0", _vp), ("dy", _vp),
+                ("dh_last", _vp), ("du", _vp), ("ddelta", _vp), ("dz", _vp), ("dA", _vp),
+                ("dB", _vp), ("dC", _vp), ("dD", _vp), ("ddelta_bias", _vp), ("dh0", _vp)]
+
+
 class Conv1dArgs(ctypes.Structure):
     """Mirror of ss_conv1d_args."""
     _fields_ = [("batch", ctypes.c_int), ("dim", ctypes.c_int), ("width", ctypes.c_int),
@@ -86,6 +96,7 @@ def lib():
             L.ss_scan_fwd.argtypes = [_vp, ctypes.POINTER(ScanArgs), _vp]
             L.ss_state_update.argtypes = [_vp, ctypes.POINTER(UpdateArgs), _vp]
             L.ss_conv1d_fwd.argtypes = [_vp, ctypes.POINTER(Conv1dArgs), _vp]
+            L.ss_scan_bwd.argtypes = [_vp, ctypes.POINTER(ScanBwdArgs), _vp]
             L.ss_conv1d_update.argtypes = [_vp, ctypes.POINTER(Conv1dUpdateArgs), _vp]
             L.ss_get_device_error.argtypes = [_vp, _vp]
             L.ss_status_string.argtypes = [ctypes.c_int]
@@ -314,6 +325,51 @@ def ss_state_update(state, x, dt, A, B, C, D=None, dt_bias=None, z=None, dt_soft
     return y
 
 
+def ss_scan_bwd(u, delta, A, B, C, dy, D=None, delta_bias=None, z=None, delta_softplus=True,
+                h0=None, dh_last=None, ctx: Context | None = None, stream=None):
+    """Gradients of the selective scan on the GPU.
+
+    Inputs as for ss_scan_fwd; dy (batch, dim, L) and dh_last (batch, dim, N)
+    float32 (dh_last may be None). Returns a dict of float32 tensors: du,
+    ddelta, dz (None without z), dA, dB, dC, dD (None without D), ddelta_bias
+    (None without delta_bias), dh0 (None without h0)."""
+    import torch
+    _need(u, "u")
+    batch, dim, L = u.shape
+    N = B.shape[1]
+    dev = u.device
+    _need(delta, "delta", u.shape, u.dtype, dev)
+    if z is not None:
+        _need(z, "z", u.shape, u.dtype, dev)
+    _need(B, "B", (batch, N, L), u.dtype, dev)
+    _need(C, "C", (batch, N, L), u.dtype, dev)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    for t, name in ((D, "D"), (delta_bias, "delta_bias")):
+        if t is not None:
+            _need(t, name, (dim,), torch.float32, dev)
+    if h0 is not None:
+        _need(h0, "h0", (batch, dim, N), torch.float32, dev)
+    _need(dy, "dy", (batch, dim, L), torch.float32, dev)
+    if dh_last is not None:
+        _need(dh_last, "dh_last", (batch, dim, N), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(du=torch.empty((batch, dim, L), **f32), ddelta=torch.empty((batch, dim, L), **f32),
+             dz=torch.empty((batch, dim, L), **f32) if z is not None else None,
+             dA=torch.empty((dim, N), **f32), dB=torch.empty((batch, N, L), **f32),
+             dC=torch.empty((batch, N, L), **f32),
+             dD=torch.empty((dim,), **f32) if D is not None else None,
+             ddelta_bias=torch.empty((dim,), **f32) if delta_bias is not None else None,
+             dh0=torch.empty((batch, dim, N), **f32) if h0 is not None else None)
+    a = ScanBwdArgs(batch, dim, N, L, _dtype_code(u), _p(u), _p(delta), _p(z), _p(A), _p(B),
+                    _p(C), _p(D), _p(delta_bias), int(bool(delta_softplus)), _p(h0), _p(dy),
+                    _p(dh_last), _p(g["du"]), _p(g["ddelta"]), _p(g["dz"]), _p(g["dA"]),
+                    _p(g["dB"]), _p(g["dC"]), _p(g["dD"]), _p(g["ddelta_bias"]), _p(g["dh0"]))
+    ctx = ctx or default_context(dev.index if dev.index is not None else 0)
+    _check(lib().ss_scan_bwd(ctx.handle, ctypes.byref(a), _stream_ptr(stream, dev)),
+           "ss_scan_bwd")
+    return g
+
+
 def ss_conv1d_fwd(x, weight, bias=None, init_state=None, silu=False, out=None,
                   final_state=None, out_dtype=None, return_final_state=True,
                   ctx: Context | None = None, stream=None):
@@ -375,6 +431,6 @@ def ss_conv1d_update(state, x, weight, bias=None, silu=False, out=None, out_dtyp
     return out
 
 
-__all__ = ["ss_scan_fwd", "ss_state_update", "ss_conv1d_fwd", "ss_conv1d_update",
+__all__ = ["ss_scan_fwd", "ss_scan_bwd", "ss_state_update", "ss_conv1d_fwd", "ss_conv1d_update",
            "PreparedScan", "Context", "SSError", "lib", "status_string",
-           "ScanArgs", "UpdateArgs", "Conv1dArgs", "Conv1dUpdateArgs", "LIB_PATH"]
+           "ScanArgs", "UpdateArgs", "ScanBwdArgs", "Conv1dArgs", "Conv1dUpdateArgs", "LIB_PATH"]

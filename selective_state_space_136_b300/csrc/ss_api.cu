@@ -112,6 +112,7 @@ int ss_destroy(ss_ctx *ctx) {
     cudaDeviceSynchronize();
     if (ctx->d_err) cudaFree(ctx->d_err);
     if (ctx->scratch) cudaFree(ctx->scratch);
+    if (ctx->bwd_scratch) cudaFree(ctx->bwd_scratch);
     cudaSetDevice(prev);
     delete ctx;
     return SS_OK;
@@ -328,6 +329,77 @@ int ss_state_update(ss_ctx *ctx, const ss_update_args *a, ss_stream_t stream) {
                         a->x, a->dt, a->z, a->A, a->B, a->C, a->D, a->dt_bias,
                         a->dt_softplus, a->y, ctx->zoh};
     const int rc = ssh::launch_update(p, reinterpret_cast<cudaStream_t>(stream));
+    ctx->last_variant = 0;
+    ctx->last_launches = rc == SS_OK ? 1 : 0;
+    return rc;
+}
+
+int ss_scan_bwd(ss_ctx *ctx, const ss_scan_bwd_args *a, ss_stream_t stream) {
+    if (!ctx || !a) return SS_ERR_INVALID_ARG;
+    if (a->batch < 1 || a->dim < 1 || a->seqlen < 1) return SS_ERR_INVALID_ARG;
+    if (!valid_dtype(a->in_dtype)) return SS_ERR_INVALID_ARG;
+    if (!valid_dstate(a->dstate)) return SS_ERR_UNSUPPORTED;
+    if ((long long)a->batch * a->dim > (1LL << 40) || a->seqlen >= (1LL << 35))
+        return SS_ERR_INVALID_ARG;
+    if (!a->u || !a->delta || !a->A || !a->B || !a->C || !a->dy || !a->du || !a->ddelta ||
+        !a->dA || !a->dB || !a->dC)
+        return SS_ERR_INVALID_ARG;
+    if (a->dz && !a->z) return SS_ERR_INVALID_ARG;
+    const void *ptrs[] = {a->u,  a->delta, a->z,  a->A,  a->B,  a->C,  a->D,  a->delta_bias,
+                          a->h0, a->dy,    a->dh_last, a->du, a->ddelta, a->dz, a->dA,
+                          a->dB, a->dC,    a->dD, a->ddelta_bias, a->dh0};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return SS_ERR_INVALID_ARG;
+    const size_t rows = (size_t)a->batch * a->dim, L = (size_t)a->seqlen, N = (size_t)a->dstate;
+    const size_t esz = a->in_dtype == SS_BF16 ? 2 : 4;
+    const Span ins[] = {span(a->u, rows * L * esz), span(a->delta, rows * L * esz),
+                        span(a->z, a->z ? rows * L * esz : 0), span(a->A, (size_t)a->dim * N * 4),
+                        span(a->B, (size_t)a->batch * N * L * esz),
+                        span(a->C, (size_t)a->batch * N * L * esz),
+                        span(a->D, a->D ? (size_t)a->dim * 4 : 0),
+                        span(a->delta_bias, a->delta_bias ? (size_t)a->dim * 4 : 0),
+                        span(a->h0, a->h0 ? rows * N * 4 : 0), span(a->dy, rows * L * 4),
+                        span(a->dh_last, a->dh_last ? rows * N * 4 : 0)};
+    const Span outs[] = {span(a->du, rows * L * 4), span(a->ddelta, rows * L * 4),
+                         span(a->dz, a->dz ? rows * L * 4 : 0), span(a->dA, (size_t)a->dim * N * 4),
+                         span(a->dB, (size_t)a->batch * N * L * 4),
+                         span(a->dC, (size_t)a->batch * N * L * 4),
+                         span(a->dD, a->dD ? (size_t)a->dim * 4 : 0),
+                         span(a->ddelta_bias, a->ddelta_bias ? (size_t)a->dim * 4 : 0),
+                         span(a->dh0, a->dh0 ? rows * N * 4 : 0)};
+    const size_t n_out = sizeof(outs) / sizeof(outs[0]);
+    for (size_t i = 0; i < n_out; ++i) {
+        for (const Span &s : ins)
+            if (overlaps(outs[i], s)) return SS_ERR_INVALID_ARG;
+        for (size_t j = i + 1; j < n_out; ++j)
+            if (overlaps(outs[i], outs[j])) return SS_ERR_INVALID_ARG;
+    }
+    if (ctx->zoh) return SS_ERR_UNSUPPORTED;
+    ssh::BwdParams p{a->batch, a->dim, a->dstate, a->seqlen, a->in_dtype, a->u, a->delta, a->z,
+                     a->A, a->B, a->C, a->D, a->delta_bias, a->delta_softplus, a->h0, a->dy,
+                     a->dh_last, a->du, a->ddelta, a->dz, a->dA, a->dB, a->dC, a->dD,
+                     a->ddelta_bias, a->dh0, nullptr};
+    if (!ssh::bwd_supported(p)) return SS_ERR_UNSUPPORTED;
+    if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
+    const size_t need = ssh::bwd_ckpt_bytes(p);
+    if (need > ctx->bwd_scratch_bytes) {
+        if (ctx->bwd_scratch) {
+            if (cudaFree(ctx->bwd_scratch) != cudaSuccess) return SS_ERR_CUDA;
+            ctx->bwd_scratch = nullptr;
+            ctx->bwd_scratch_bytes = 0;
+        }
+        if (cudaMalloc(&ctx->bwd_scratch, need) != cudaSuccess) return SS_ERR_CUDA;
+        ctx->bwd_scratch_bytes = need;
+    }
+    p.ckpt = static_cast<float *>(ctx->bwd_scratch);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the sums over rows start from zero
+    float *sums[] = {a->dA, a->dB, a->dC, a->dD, a->ddelta_bias};
+    const size_t sum_b[] = {(size_t)a->dim * N * 4, (size_t)a->batch * N * L * 4,
+                            (size_t)a->batch * N * L * 4, (size_t)a->dim * 4, (size_t)a->dim * 4};
+    for (int i = 0; i < 5; ++i)
+        if (sums[i] && cudaMemsetAsync(sums[i], 0, sum_b[i], st) != cudaSuccess) return SS_ERR_CUDA;
+    const int rc = ssh::launch_bwd(p, st);
     ctx->last_variant = 0;
     ctx->last_launches = rc == SS_OK ? 1 : 0;
     return rc;

@@ -1,0 +1,322 @@
+// Backward pass of the selective scan: gradients of every input from dy (and
+// optionally dh_last), by recomputation.
+//
+// "Mamba: Linear-Time Sequence Modeling with Selective State Spaces", section
+// "Hardware-aware state expansion": the expanded states are not stored for
+// the backward pass but recomputed on chip from the inputs. Here a forward
+// sweep keeps only the state entering every tile of 16 steps (a checkpoint,
+// N floats per row and tile, in the context scratch); the reverse sweep then
+// recomputes each half tile's 8 states into shared memory from its checkpoint
+// and walks them backwards.
+//
+// Reverse step t of a row (g = dL/dh(t), the adjoint state, in registers):
+//     s = sum_n C_n h_n(t) + D u,  gs = dy silu(z),  dz = dy s silu'(z)
+//     g_n += gs C_n;   dC_n(t) += gs h_n(t);   dB_n(t) += g_n dt u
+//     du = gs D + sum_n g_n dt B_n;   ddt = sum_n g_n (A_n e_n h_n(t-1) + B_n u)
+//     dA_n += g_n dt e_n h_n(t-1);    g_n *= e_n
+//     ddelta = ddt sigmoid(delta + bias) (softplus on), dbias += ddelta, dD += gs u
+// dB and dC are sums over every channel of a batch: each warp (32 rows of one
+// batch) sums its rows through a shared-memory transpose and adds the 2N sums
+// of a step to global memory atomically. dA, dD, dbias are per-row sums added
+// once per row at the end.
+//
+// Layout: one warp per row block (32 channels of one batch), one thread per
+// row with all N states in registers.
+#include "ss_common.cuh"
+#include "ss_internal.h"
+
+namespace {
+
+using namespace ssk;
+
+constexpr int kTL = 16;   // steps per tile (checkpoint spacing)
+constexpr int kHalf = 8;  // steps recomputed into shared memory at a time
+
+template <int N>
+struct BwdSmem {
+    float bc[kTL][2 * N];          // this tile's B (n < N) and C (n >= N), fp32
+    float S[kHalf][N][32];         // recomputed states h_n(t) of each lane
+    float red[32][2 * N + 1];      // per-lane dB/dC terms of one step (padded)
+    float out[3][kTL][32];         // du, ddelta, dz of the tile, per lane
+    float in[5][kTL][32];          // dt, u, sigmoid(delta + bias), z, dy of the tile, per lane
+};
+
+// This lane's row: TL inputs of a tile as fp32.
+__device__ __forceinline__ void load_tile(const uint16_t *p, float *v) {
+#pragma unroll
+    for (int c = 0; c < kTL / 8; ++c) {
+        const uint4 t = *reinterpret_cast<const uint4 *>(p + 8 * c);
+        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[8 * c + 2 * k] = bf16lo(w[k]), v[8 * c + 2 * k + 1] = bf16hi(w[k]);
+    }
+}
+__device__ __forceinline__ void load_tile(const float *p, float *v) {
+#pragma unroll
+    for (int c = 0; c < kTL / 4; ++c) {
+        const float4 t = *reinterpret_cast<const float4 *>(p + 4 * c);
+        v[4 * c] = t.x, v[4 * c + 1] = t.y, v[4 * c + 2] = t.z, v[4 * c + 3] = t.w;
+    }
+}
+__device__ __forceinline__ void store_tile16(float *p, const float *v) {
+#pragma unroll
+    for (int c = 0; c < kTL / 4; ++c)
+        *reinterpret_cast<float4 *>(p + 4 * c) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
+
+// The warp loads the tile's B and C (batch b, steps l0 .. l0+15) into bc,
+// widened to fp32: lane i < 2N reads row n = i % N of B (i < N) or C.
+template <typename Tin, int N>
+__device__ __forceinline__ void load_bc(BwdSmem<N> &sm, const ssh::BwdParams &p, int b, long long l0,
+                                        int lane) {
+    __syncwarp();
+    if (lane < 2 * N) {
+        const int n = lane % N;
+        const Tin *src = static_cast<const Tin *>(lane < N ? p.B : p.C) +
+                         ((long long)b * N + n) * p.seqlen + l0;
+        float v[kTL];
+        load_tile(src, v);
+#pragma unroll
+        for (int t = 0; t < kTL; ++t) sm.bc[t][lane] = v[t];
+    }
+    __syncwarp();
+}
+
+template <typename Tin, int N>
+__global__ void __launch_bounds__(32) scan_bwd_kernel(const ssh::BwdParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    BwdSmem<N> &sm = *reinterpret_cast<BwdSmem<N> *>(smem_raw);
+    const int lane = threadIdx.x;
+    const int rb_per_batch = (p.dim + 31) / 32;
+    const int b = blockIdx.x / rb_per_batch, blk = blockIdx.x % rb_per_batch;
+    const int d = blk * 32 + lane;
+    const bool row_ok = d < p.dim;
+    const int dc = row_ok ? d : p.dim - 1;
+    const long long row = (long long)b * p.dim + dc;
+    const long long L = p.seqlen;
+    const int K = (int)(L / kTL);
+
+    float A2[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) A2[n] = p.A[(long long)dc * N + n] * kLog2e;
+    const float bias = p.bias ? p.bias[dc] : 0.f;
+    const float Dd = p.D ? p.D[dc] : 0.f;
+    const Tin *gu = static_cast<const Tin *>(p.u) + row * L;
+    const Tin *gd = static_cast<const Tin *>(p.delta) + row * L;
+    const Tin *gz = p.z ? static_cast<const Tin *>(p.z) + row * L : nullptr;
+    // checkpoints by the lane's slot in the padded row grid (rows past dim too)
+    float *ck = p.ckpt + ((long long)blockIdx.x * 32 + lane) * (long long)K * N;
+
+    // dt and dt*u of a tile for this lane's row
+    auto tile_dt = [&](long long l0, float *dt, float *uv, float *xv) {
+        float dl[kTL];
+        load_tile(gu + l0, uv);
+        load_tile(gd + l0, dl);
+#pragma unroll
+        for (int t = 0; t < kTL; ++t) {
+            xv[t] = dl[t] + bias;
+            dt[t] = p.softplus ? softplus1(xv[t]) : xv[t];
+        }
+    };
+    auto fwd_step = [&](float *h, float dt, float du, int t) {
+#pragma unroll
+        for (int n = 0; n < N; ++n) h[n] = fmaf(ex2(dt * A2[n]), h[n], du * sm.bc[t][n]);
+    };
+
+    // ---- forward sweep: the state entering every tile
+    float h[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) h[n] = p.h0 ? p.h0[row * N + n] : 0.f;
+    for (int k = 0; k < K; ++k) {
+        const long long l0 = (long long)k * kTL;
+#pragma unroll
+        for (int n = 0; n < N; ++n) ck[(long long)k * N + n] = h[n];
+        load_bc<Tin, N>(sm, p, b, l0, lane);
+        float dt[kTL], uv[kTL], xv[kTL];
+        tile_dt(l0, dt, uv, xv);
+#pragma unroll
+        for (int t = 0; t < kTL; ++t) fwd_step(h, dt[t], dt[t] * uv[t], t);
+    }
+
+    // ---- reverse sweep
+    float g[N], gA[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        g[n] = (row_ok && p.dh_last) ? p.dh_last[row * N + n] : 0.f;
+        gA[n] = 0.f;
+    }
+    float gD = 0.f, gbias = 0.f;
+    for (int k = K - 1; k >= 0; --k) {
+        const long long l0 = (long long)k * kTL;
+        load_bc<Tin, N>(sm, p, b, l0, lane);
+        {
+            float dt[kTL], uv[kTL], xv[kTL], v[kTL];
+            tile_dt(l0, dt, uv, xv);
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) {
+                sm.in[0][t][lane] = dt[t];
+                sm.in[1][t][lane] = uv[t];
+                sm.in[2][t][lane] = __fdividef(1.f, 1.f + ex2(-xv[t] * kLog2e));
+            }
+            if (gz) {
+                load_tile(gz + l0, v);
+#pragma unroll
+                for (int t = 0; t < kTL; ++t) sm.in[3][t][lane] = v[t];
+            }
+            load_tile(p.dy + row * L + l0, v);
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) sm.in[4][t][lane] = row_ok ? v[t] : 0.f;  // rows past dim add nothing
+        }
+        __syncwarp();
+        float hc[N];  // checkpoint: the state entering the tile
+#pragma unroll
+        for (int n = 0; n < N; ++n) hc[n] = ck[(long long)k * N + n];
+
+#pragma unroll 1
+        for (int half = 1; half >= 0; --half) {
+            const int t0 = half * kHalf;
+            // recompute the states of this half tile into S (h before it in hp)
+            float hp[N];
+#pragma unroll
+            for (int n = 0; n < N; ++n) hp[n] = hc[n];
+            if (half == 1) {
+#pragma unroll
+                for (int t = 0; t < kHalf; ++t) {
+                    const float dtt = sm.in[0][t][lane];
+                    fwd_step(hp, dtt, dtt * sm.in[1][t][lane], t);
+                }
+            }
+            {
+                float hh[N];
+#pragma unroll
+                for (int n = 0; n < N; ++n) hh[n] = hp[n];
+#pragma unroll
+                for (int t = 0; t < kHalf; ++t) {
+                    const float dtt = sm.in[0][t0 + t][lane];
+                    fwd_step(hh, dtt, dtt * sm.in[1][t0 + t][lane], t0 + t);
+#pragma unroll
+                    for (int n = 0; n < N; ++n) sm.S[t][n][lane] = hh[n];
+                }
+            }
+            // walk the half tile backwards
+#pragma unroll
+            for (int t = kHalf - 1; t >= 0; --t) {
+                const int tt = t0 + t;
+                const float dtt = sm.in[0][tt][lane], u = sm.in[1][tt][lane];
+                const float dyt = sm.in[4][tt][lane];
+                float s = Dd * u;
+#pragma unroll
+                for (int n = 0; n < N; ++n) s = fmaf(sm.bc[tt][N + n], sm.S[t][n][lane], s);
+                float gs = dyt;
+                if (gz) {
+                    const float zz = sm.in[3][tt][lane];
+                    const float sg = __fdividef(1.f, 1.f + ex2(-zz * kLog2e));
+                    sm.out[2][tt][lane] = dyt * s * sg * fmaf(zz, 1.f - sg, 1.f);
+                    gs = dyt * zz * sg;
+                }
+                gD = fmaf(gs, u, gD);
+                float gu_ = gs * Dd, gdt = 0.f;
+#pragma unroll
+                for (int n = 0; n < N; ++n) {
+                    const float Bn = sm.bc[tt][n], Cn = sm.bc[tt][N + n];
+                    const float hprev = t > 0 ? sm.S[t - 1][n][lane] : hp[n];
+                    const float e = ex2(dtt * A2[n]);
+                    g[n] = fmaf(gs, Cn, g[n]);
+                    sm.red[lane][N + n] = gs * sm.S[t][n][lane];
+                    const float gdu = g[n] * dtt;
+                    sm.red[lane][n] = gdu * u;
+                    gu_ = fmaf(gdu, Bn, gu_);
+                    const float ehp = e * hprev;
+                    gdt = fmaf(g[n], fmaf(A2[n] * kLn2, ehp, Bn * u), gdt);
+                    gA[n] = fmaf(gdu, ehp, gA[n]);
+                    g[n] *= e;
+                }
+                const float gx = p.softplus ? gdt * sm.in[2][tt][lane] : gdt;
+                gbias += gx;
+                sm.out[0][tt][lane] = gu_;
+                sm.out[1][tt][lane] = gx;
+                // dB and dC of step l0 + tt: sum over the warp's rows, add to global
+                __syncwarp();
+                if (lane < 2 * N) {
+                    float acc = 0.f;
+#pragma unroll 8
+                    for (int j = 0; j < 32; ++j) acc += sm.red[j][lane];
+                    const int n = lane % N;
+                    float *dst = (lane < N ? p.dB : p.dC) + ((long long)b * N + n) * L + l0 + tt;
+                    atomicAdd(dst, acc);
+                }
+                __syncwarp();
+            }
+        }
+        __syncwarp();
+        if (row_ok) {
+            float v[kTL];
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) v[t] = sm.out[0][t][lane];
+            store_tile16(p.du + row * L + l0, v);
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) v[t] = sm.out[1][t][lane];
+            store_tile16(p.ddelta + row * L + l0, v);
+            if (p.dz) {
+#pragma unroll
+                for (int t = 0; t < kTL; ++t) v[t] = sm.out[2][t][lane];
+                store_tile16(p.dz + row * L + l0, v);
+            }
+        }
+    }
+    if (row_ok) {
+        if (p.dh0) {
+#pragma unroll
+            for (int n = 0; n < N; ++n) p.dh0[row * N + n] = g[n];
+        }
+#pragma unroll
+        for (int n = 0; n < N; ++n) atomicAdd(p.dA + (long long)dc * N + n, gA[n]);
+        if (p.dD) atomicAdd(p.dD + dc, gD);
+        if (p.dbias) atomicAdd(p.dbias + dc, gbias);
+    }
+}
+
+template <typename Tin, int N>
+int bwd_n(const ssh::BwdParams &p, cudaStream_t st) {
+    const int smem = (int)sizeof(BwdSmem<N>);
+    auto kern = scan_bwd_kernel<Tin, N>;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return SS_ERR_CUDA;
+        attr_done[dev] = true;
+    }
+    const long long blocks = (long long)p.batch * ((p.dim + 31) / 32);
+    kern<<<(unsigned)blocks, 32, smem, st>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+template <typename Tin>
+int bwd_t(const ssh::BwdParams &p, cudaStream_t st) {
+    switch (p.dstate) {
+        case 1: return bwd_n<Tin, 1>(p, st);
+        case 2: return bwd_n<Tin, 2>(p, st);
+        case 4: return bwd_n<Tin, 4>(p, st);
+        case 8: return bwd_n<Tin, 8>(p, st);
+        case 16: return bwd_n<Tin, 16>(p, st);
+        default: return SS_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+size_t ssh::bwd_ckpt_bytes(const ssh::BwdParams &p) {
+    return (size_t)p.batch * (size_t)((p.dim + 31) / 32) * 32 * (size_t)(p.seqlen / kTL) *
+           (size_t)p.dstate * sizeof(float);
+}
+
+bool ssh::bwd_supported(const ssh::BwdParams &p) {
+    return p.seqlen % kTL == 0 && p.seqlen / kTL < (1LL << 31);
+}
+
+int ssh::launch_bwd(const ssh::BwdParams &p, cudaStream_t st) {
+    return p.in_dtype == SS_BF16 ? bwd_t<uint16_t>(p, st) : bwd_t<float>(p, st);
+}

@@ -23,6 +23,8 @@ struct ss_ctx {
     uint32_t wait_limit = 1u << 22;  // polls before a device wait gives up
     int drop_tile = -1;            // test hook: a tile whose loads are never issued
     int zoh = 0;                   // SS_DISC_ZOH: exact zero-order-hold input matrix
+    void *bwd_scratch = nullptr;   // backward checkpoints, grown on demand
+    size_t bwd_scratch_bytes = 0;
     int last_variant = 0;
     int last_launches = 0;
 };
@@ -92,6 +94,25 @@ struct UpdateParams {
     int zoh;
 };
 int launch_update(const UpdateParams &p, cudaStream_t st);
+
+// backward pass (ss_bwd.cu)
+struct BwdParams {
+    int batch, dim, dstate;
+    long long seqlen;
+    int in_dtype;
+    const void *u, *delta, *z;
+    const float *A;
+    const void *B, *C;
+    const float *D, *bias;
+    int softplus;
+    const float *h0;
+    const float *dy, *dh_last;
+    float *du, *ddelta, *dz, *dA, *dB, *dC, *dD, *dbias, *dh0;
+    float *ckpt;  // scratch: bwd_ckpt_bytes
+};
+size_t bwd_ckpt_bytes(const BwdParams &p);
+bool bwd_supported(const BwdParams &p);
+int launch_bwd(const BwdParams &p, cudaStream_t st);
 
 // causal depthwise conv1d (ss_conv.cu)
 struct ConvParams {
