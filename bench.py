@@ -267,10 +267,22 @@ def time_decode(ss, ctx, dev, stream, args, n_sets=6):
         y = torch.empty((cfg.batch, cfg.dim), dtype=torch.float32, device=dev)
         sets.append((st, inp, y))
 
+    # each step's arguments marshalled once (a decode step is shorter than the
+    # Python checks of the per-call binding)
+    import ctypes
+    fn = ss.lib().ss_state_update
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    prepared = []
+    for st, inp, y in sets:
+        a = ss.UpdateArgs(cfg.batch, cfg.dim, cfg.dstate, 1, 0, st.data_ptr(), inp["x"].data_ptr(),
+                          inp["dt"].data_ptr(), inp["z"].data_ptr(), A.data_ptr(),
+                          inp["B"].data_ptr(), inp["C"].data_ptr(), Dp.data_ptr(),
+                          bias.data_ptr(), 1, y.data_ptr())
+        prepared.append((a, ctypes.byref(a)))
+
     def one(k):
-        st, inp, y = sets[k % n_sets]
-        ss.ss_state_update(st, inp["x"], inp["dt"], A, inp["B"], inp["C"], D=Dp, dt_bias=bias,
-                           z=inp["z"], y=y, ctx=ctx, stream=stream)
+        if fn(ctx.handle, prepared[k % n_sets][1], sp) != 0:
+            raise RuntimeError("ss_state_update failed")
 
     for k in range(max(args.warmup, 3) * n_sets):
         one(k)
