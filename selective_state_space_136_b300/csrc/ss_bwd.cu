@@ -16,8 +16,8 @@
 //     dA_n += g_n dt e_n h_n(t-1);    g_n *= e_n
 //     ddelta = ddt sigmoid(delta + bias) (softplus on), dbias += ddelta, dD += gs u
 // dB and dC are sums over every channel of a batch: each warp (32 rows of one
-// batch) sums its rows through a shared-memory transpose and adds the 2N sums
-// of a step to global memory atomically. dA, dD, dbias are per-row sums added
+// batch) sums its rows by a shuffle reduce-scatter and adds the 2N sums of a
+// step to global memory atomically. dA, dD, dbias are per-row sums added
 // once per row at the end.
 //
 // Layout: one warp per row block (32 channels of one batch), one thread per
@@ -36,7 +36,6 @@ template <int N>
 struct BwdSmem {
     float bc[kTL][2 * N];          // this tile's B (n < N) and C (n >= N), fp32
     float S[kHalf][N][32];         // recomputed states h_n(t) of each lane
-    float red[32][2 * N + 1];      // per-lane dB/dC terms of one step (padded)
     float out[3][kTL][32];         // du, ddelta, dz of the tile, per lane
     float in[5][kTL][32];          // dt, u, sigmoid(delta + bias), z, dy of the tile, per lane
 };
@@ -198,15 +197,22 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ssh::BwdParams p) {
                     for (int n = 0; n < N; ++n) sm.S[t][n][lane] = hh[n];
                 }
             }
-            // walk the half tile backwards
+            // walk the half tile backwards; hcur = h(t), loaded once per step as
+            // the previous step's h(t-1)
+            float hcur[N];
+#pragma unroll
+            for (int n = 0; n < N; ++n) hcur[n] = sm.S[kHalf - 1][n][lane];
 #pragma unroll
             for (int t = kHalf - 1; t >= 0; --t) {
                 const int tt = t0 + t;
                 const float dtt = sm.in[0][tt][lane], u = sm.in[1][tt][lane];
                 const float dyt = sm.in[4][tt][lane];
+                float hprev[N];
+#pragma unroll
+                for (int n = 0; n < N; ++n) hprev[n] = t > 0 ? sm.S[t - 1][n][lane] : hp[n];
                 float s = Dd * u;
 #pragma unroll
-                for (int n = 0; n < N; ++n) s = fmaf(sm.bc[tt][N + n], sm.S[t][n][lane], s);
+                for (int n = 0; n < N; ++n) s = fmaf(sm.bc[tt][N + n], hcur[n], s);
                 float gs = dyt;
                 if (gz) {
                     const float zz = sm.in[3][tt][lane];
@@ -216,36 +222,49 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ssh::BwdParams p) {
                 }
                 gD = fmaf(gs, u, gD);
                 float gu_ = gs * Dd, gdt = 0.f;
+                float v[2 * N];  // this row's dB (n < N) and dC terms of the step
 #pragma unroll
                 for (int n = 0; n < N; ++n) {
                     const float Bn = sm.bc[tt][n], Cn = sm.bc[tt][N + n];
-                    const float hprev = t > 0 ? sm.S[t - 1][n][lane] : hp[n];
                     const float e = ex2(dtt * A2[n]);
                     g[n] = fmaf(gs, Cn, g[n]);
-                    sm.red[lane][N + n] = gs * sm.S[t][n][lane];
+                    v[N + n] = gs * hcur[n];
                     const float gdu = g[n] * dtt;
-                    sm.red[lane][n] = gdu * u;
+                    v[n] = gdu * u;
                     gu_ = fmaf(gdu, Bn, gu_);
-                    const float ehp = e * hprev;
+                    const float ehp = e * hprev[n];
                     gdt = fmaf(g[n], fmaf(A2[n] * kLn2, ehp, Bn * u), gdt);
                     gA[n] = fmaf(gdu, ehp, gA[n]);
                     g[n] *= e;
+                    hcur[n] = hprev[n];
                 }
                 const float gx = p.softplus ? gdt * sm.in[2][tt][lane] : gdt;
                 gbias += gx;
                 sm.out[0][tt][lane] = gu_;
                 sm.out[1][tt][lane] = gx;
-                // dB and dC of step l0 + tt: sum over the warp's rows, add to global
-                __syncwarp();
+                // dB and dC of the step summed over the warp's 32 rows by a
+                // shuffle reduce-scatter: full sums across lane bits >= 2N, then
+                // recursive halving, after which lane L holds value L % 2N
+                constexpr unsigned FULL = 0xffffffffu;
+#pragma unroll
+                for (int w = 16; w >= 2 * N; w >>= 1)
+#pragma unroll
+                    for (int i = 0; i < 2 * N; ++i) v[i] += __shfl_xor_sync(FULL, v[i], w);
+#pragma unroll
+                for (int w = (2 * N < 32 ? N : 16); w >= 1; w >>= 1) {
+                    const bool upper = (lane & w) != 0;
+#pragma unroll
+                    for (int i = 0; i < w; ++i) {
+                        const float send = upper ? v[i] : v[i + w];
+                        const float keep = upper ? v[i + w] : v[i];
+                        v[i] = keep + __shfl_xor_sync(FULL, send, w);
+                    }
+                }
                 if (lane < 2 * N) {
-                    float acc = 0.f;
-#pragma unroll 8
-                    for (int j = 0; j < 32; ++j) acc += sm.red[j][lane];
                     const int n = lane % N;
                     float *dst = (lane < N ? p.dB : p.dC) + ((long long)b * N + n) * L + l0 + tt;
-                    atomicAdd(dst, acc);
+                    atomicAdd(dst, v[0]);
                 }
-                __syncwarp();
             }
         }
         __syncwarp();
