@@ -19,6 +19,9 @@
 #ifndef SS_UPD_TPR16
 #define SS_UPD_TPR16 4  // threads per row for dstate 16
 #endif
+#ifndef SS_UPD_RPT
+#define SS_UPD_RPT 1  // rows per thread group (2 measured the same, 4 slower)
+#endif
 
 namespace {
 
@@ -81,50 +84,63 @@ __device__ __forceinline__ float gate(float z, uint16_t) {
     return g.x;
 }
 
-template <typename Tin, typename Tout, int N, int TPR>
+template <typename Tin, typename Tout, int N, int TPR, int RPT>
 __global__ void __launch_bounds__(256) state_update_kernel(const ssh::UpdateParams p) {
     constexpr int NS = N / TPR;
-    const long long rows = (long long)p.batch * p.dim;
-    const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long row_raw = g / TPR;
+    const uint32_t rows = (uint32_t)p.batch * (uint32_t)p.dim;
+    const uint32_t g = blockIdx.x * blockDim.x + threadIdx.x;
     const int q = (int)(g % TPR);
-    const bool ok = row_raw < rows;
-    // threads past the end keep running on row 0 so the shuffles stay full-warp
-    const long long row = ok ? row_raw : 0;
-    // 32-bit division (the launcher keeps batch * dim * TPR below 2^31)
-    const uint32_t bq = (uint32_t)row / (uint32_t)p.dim;
-    const int b = (int)bq, d = (int)((uint32_t)row - bq * (uint32_t)p.dim);
-
-    float st[NS], A[NS], Bv[NS], Cv[NS];
-    ld_f32<NS>(p.state + row * N + q * NS, st);
-    const float xv = to_f32(static_cast<const Tin *>(p.x)[row]);
-    const float xr = to_f32(static_cast<const Tin *>(p.dt)[row]) + (p.bias ? p.bias[d] : 0.f);
-    ld_f32<NS>(p.A + (long long)d * N + q * NS, A);
-    ld_in<NS>(static_cast<const Tin *>(p.B) + (long long)b * N + q * NS, Bv);
-    ld_in<NS>(static_cast<const Tin *>(p.C) + (long long)b * N + q * NS, Cv);
-    const float dt = p.softplus ? softplus1(xr) : xr;
-    const float dtx = dt * xv;
-    float acc = 0.f;
+    // RPT rows per thread group, one grid-width of groups apart, so every
+    // warp access stays contiguous; all loads of all RPT rows are issued
+    // before any arithmetic
+    const uint32_t span = gridDim.x * blockDim.x / TPR;
+    float st[RPT][NS], A[RPT][NS], Bv[RPT][NS], Cv[RPT][NS], xv[RPT], xr[RPT], zv[RPT], Dd[RPT];
+    uint32_t row[RPT];
+    bool ok[RPT];
 #pragma unroll
-    for (int i = 0; i < NS; ++i) {
-        if (p.zoh) {
-            float e;
-            const float f = zoh_step(dt, A[i], &e);
-            st[i] = fmaf(e, st[i], f * xv * Bv[i]);
-        } else {
-            const float e = ex2(dt * (A[i] * kLog2e));
-            st[i] = fmaf(e, st[i], dtx * Bv[i]);
-        }
-        acc = fmaf(Cv[i], st[i], acc);
+    for (int k = 0; k < RPT; ++k) {
+        const uint32_t rr = g / TPR + k * span;
+        ok[k] = rr < rows;
+        // threads past the end keep running on row 0 so the shuffles stay full-warp
+        row[k] = ok[k] ? rr : 0u;
+        const uint32_t bq = row[k] / (uint32_t)p.dim;
+        const int b = (int)bq, d = (int)(row[k] - bq * (uint32_t)p.dim);
+        ld_f32<NS>(p.state + (long long)row[k] * N + q * NS, st[k]);
+        xv[k] = to_f32(static_cast<const Tin *>(p.x)[row[k]]);
+        xr[k] = to_f32(static_cast<const Tin *>(p.dt)[row[k]]) + (p.bias ? p.bias[d] : 0.f);
+        zv[k] = p.z ? to_f32(static_cast<const Tin *>(p.z)[row[k]]) : 0.f;
+        Dd[k] = p.D ? p.D[d] : 0.f;
+        ld_f32<NS>(p.A + (long long)d * N + q * NS, A[k]);
+        ld_in<NS>(static_cast<const Tin *>(p.B) + (long long)b * N + q * NS, Bv[k]);
+        ld_in<NS>(static_cast<const Tin *>(p.C) + (long long)b * N + q * NS, Cv[k]);
     }
 #pragma unroll
-    for (int m = TPR / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-    if (!ok) return;
-    st_f32<NS>(p.state + row * N + q * NS, st);
-    if (q == 0) {
-        float o = fmaf(p.D ? p.D[d] : 0.f, xv, acc);
-        if (p.z) o *= gate(to_f32(static_cast<const Tin *>(p.z)[row]), Tin());
-        store_out(static_cast<Tout *>(p.y) + row, o);
+    for (int k = 0; k < RPT; ++k) {
+        const float dt = p.softplus ? softplus1(xr[k]) : xr[k];
+        const float dtx = dt * xv[k];
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < NS; ++i) {
+            if (p.zoh) {
+                float e;
+                const float f = zoh_step(dt, A[k][i], &e);
+                st[k][i] = fmaf(e, st[k][i], f * xv[k] * Bv[k][i]);
+            } else {
+                const float e = ex2(dt * (A[k][i] * kLog2e));
+                st[k][i] = fmaf(e, st[k][i], dtx * Bv[k][i]);
+            }
+            acc = fmaf(Cv[k][i], st[k][i], acc);
+        }
+#pragma unroll
+        for (int m = TPR / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+        if (ok[k]) {
+            st_f32<NS>(p.state + (long long)row[k] * N + q * NS, st[k]);
+            if (q == 0) {
+                float o = fmaf(Dd[k], xv[k], acc);
+                if (p.z) o *= gate(zv[k], Tin());
+                store_out(static_cast<Tout *>(p.y) + row[k], o);
+            }
+        }
     }
 }
 
@@ -132,16 +148,17 @@ template <typename Tin, typename Tout>
 int launch_n(const ssh::UpdateParams &p, cudaStream_t st) {
     const long long rows = (long long)p.batch * p.dim;
     if (rows * 16 >= (1LL << 31)) return SS_ERR_UNSUPPORTED;
+    constexpr int R = SS_UPD_RPT;
     auto go = [&](auto kern, int tpr) {
-        const long long threads = rows * tpr;
-        kern<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(p);
+        const long long groups = (rows + R - 1) / R;
+        kern<<<(unsigned)((groups * tpr + 255) / 256), 256, 0, st>>>(p);
     };
     switch (p.dstate) {
-        case 1: go(state_update_kernel<Tin, Tout, 1, 1>, 1); break;
-        case 2: go(state_update_kernel<Tin, Tout, 2, 1>, 1); break;
-        case 4: go(state_update_kernel<Tin, Tout, 4, 1>, 1); break;
-        case 8: go(state_update_kernel<Tin, Tout, 8, 2>, 2); break;
-        case 16: go(state_update_kernel<Tin, Tout, 16, SS_UPD_TPR16>, SS_UPD_TPR16); break;
+        case 1: go(state_update_kernel<Tin, Tout, 1, 1, R>, 1); break;
+        case 2: go(state_update_kernel<Tin, Tout, 2, 1, R>, 1); break;
+        case 4: go(state_update_kernel<Tin, Tout, 4, 1, R>, 1); break;
+        case 8: go(state_update_kernel<Tin, Tout, 8, 2, R>, 2); break;
+        case 16: go(state_update_kernel<Tin, Tout, 16, SS_UPD_TPR16, R>, SS_UPD_TPR16); break;
         default: return SS_ERR_UNSUPPORTED;
     }
     return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
