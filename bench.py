@@ -61,6 +61,7 @@ def parse():
     ap.add_argument("--skip-decode", action="store_true", help="skip the decode-step leg")
     ap.add_argument("--skip-conv", action="store_true", help="skip the conv1d leg")
     ap.add_argument("--skip-bwd", action="store_true", help="skip the backward leg")
+    ap.add_argument("--skip-ssd", action="store_true", help="skip the Mamba-2 SSD leg")
     return ap.parse_args()
 
 
@@ -402,6 +403,62 @@ def time_bwd(ss, ctx, dev, stream, cfg, d, params, args):
             "hbm_peak_source": src, "steps": steps, "gpu_launches": steps}
 
 
+def time_ssd(ss, ctx, dev, stream, args, batch=8, L=2048, H=80, P=64, N=128):
+    """Time ss_ssd_fwd on the Mamba-2 block shape (d_inner 5120 = 80 heads of
+    64, d_state 128), bf16 inputs, fp32 y."""
+    import ctypes
+    import torch
+    g = torch.Generator(device="cpu").manual_seed(7)
+    bf = torch.bfloat16
+    x = torch.randn((batch, L, H, P), generator=g).to(bf).to(dev)
+    dt = (torch.randn((batch, L, H), generator=g) * 0.5 - 1.0).to(bf).to(dev)
+    Bm = (torch.randn((batch, L, N), generator=g) * 0.3).to(bf).to(dev)
+    Cm = (torch.randn((batch, L, N), generator=g) * 0.3).to(bf).to(dev)
+    A = -(torch.rand((H,), generator=g) * 3.5 + 0.5).to(dev)
+    D = torch.randn((H,), generator=g).to(dev)
+    bias = torch.full((H,), -4.0).to(dev)
+    y = torch.empty((batch, L, H, P), device=dev)
+    hl = torch.empty((batch, H, P, N), device=dev)
+    a = ss.SsdArgs(batch, H, P, N, L, 1, 0, x.data_ptr(), dt.data_ptr(), A.data_ptr(),
+                   Bm.data_ptr(), Cm.data_ptr(), D.data_ptr(), bias.data_ptr(), 1, None,
+                   y.data_ptr(), hl.data_ptr())
+    fn, argp = ss.lib().ss_ssd_fwd, ctypes.byref(a)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    for _ in range(max(args.warmup, 3)):
+        assert fn(ctx.handle, argp, sp) == 0
+    torch.cuda.synchronize(dev)
+    steps = max(args.steps, 1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn(ctx.handle, argp, sp)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    Q = 64
+    chunks = batch * H * (L // Q)
+    # per chunk and head: C B^T (2 Q Q N), masked products with x (2 Q Q P),
+    # C H_prev^T (2 Q P N), B^T x~ (2 N P Q)
+    flops = chunks * (2 * Q * Q * N + 2 * Q * Q * P + 2 * Q * P * N + 2 * N * P * Q)
+    tflops = flops / (us * 1e-6) / 1e12
+    nbytes = batch * L * (H * P * 2 + H * P * 4 + H * 2 + 2 * N * 2) + 2 * batch * H * P * N * 4
+    peak_t = None
+    try:
+        peak_t = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
+    except Exception:
+        peak_t = 1800.0
+    hbm, src = measured_peaks()
+    return {"workload": "ssd (Mamba-2): batch %d, L %d, %d heads x %d, d_state %d, bf16 in, "
+                        "fp32 y, chunk %d" % (batch, L, H, P, N, Q),
+            "us_per_call": us, "elements_per_s": batch * L * H * P / (us * 1e-6),
+            "tensor": {"achieved_tflops": tflops, "peak_tflops": peak_t,
+                       "frac": tflops / peak_t, "note": "algorithmic bf16 products (the state's "
+                       "low bf16 half in C H_prev adds 2 Q P N per chunk, not counted)"},
+            "hbm": {"gbs": nbytes / (us * 1e-6) / 1e9, "peak": hbm, "peak_source": src,
+                    "frac": nbytes / (us * 1e-6) / 1e9 / hbm},
+            "steps": steps, "gpu_launches": steps}
+
+
 def run_ours(args, rank, world, local):
     import torch
     import selective_state_space_136_b300 as ss
@@ -495,6 +552,7 @@ def run_ours(args, rank, world, local):
     decode = None if args.skip_decode else time_decode(ss, ctx, dev, stream, args)
     conv1d = None if args.skip_conv else time_conv1d(ss, ctx, dev, stream, cfg, args)
     bwd = None if args.skip_bwd else time_bwd(ss, ctx, dev, stream, cfg, d, params, args)
+    ssd = None if args.skip_ssd else time_ssd(ss, ctx, dev, stream, args)
 
     # ---- end to end: pinned host inputs in, y and h_last back to host, every step
     e2e = None
@@ -613,6 +671,7 @@ def run_ours(args, rank, world, local):
         "decode": decode,
         "conv1d": conv1d,
         "backward": bwd,
+        "ssd": ssd,
         "impl": "ours",
     }
     print(json.dumps(out), flush=True)

@@ -176,6 +176,42 @@ typedef struct {
 int ss_scan_bwd(ss_ctx *ctx, const ss_scan_bwd_args *args, ss_stream_t stream);
 
 /*
+ * Mamba-2 state space duality (SSD) forward: the selective scan with a scalar
+ * decay per head, computed chunk by chunk (64 steps) with matrix products on
+ * the tensor cores (soft186.com, "Mamba选择性状态空间机制", section
+ * "状态空间对偶性算法突破": Mamba-2 computes the scan through a block
+ * decomposition of its semiseparable matrix). Per batch b, head h, channel p:
+ *     dt   = softplus(dt_raw[b,l,h] + dt_bias[h])      (or the sum itself)
+ *     H_pn = exp(dt A[h]) H_pn + dt x[b,l,h,p] B[b,l,n]
+ *     y[b,l,h,p] = sum_n C[b,l,n] H_pn + D[h] x[b,l,h,p]
+ * which is ss_scan_fwd with A constant over states and heads' channels, dt
+ * shared by a head's channels, and B, C shared by all heads (one group).
+ *   x, y   : (batch, seqlen, heads, headdim), x bf16, y fp32 or bf16.
+ *   dt     : (batch, seqlen, heads) bf16.   A, D, dt_bias: (heads) fp32 (D,
+ *            dt_bias may be NULL).   B, C: (batch, seqlen, dstate) bf16.
+ *   h0, h_last: (batch, heads, headdim, dstate) fp32 or NULL (zero start / not
+ *            written); h_last may equal h0.
+ *   headdim must be 64, dstate 64 or 128, seqlen a multiple of 64 and the
+ *   inputs bf16, else SS_ERR_UNSUPPORTED. The products run in bf16 with fp32
+ *   accumulation (the state carried between chunks in fp32).
+ */
+typedef struct {
+    int batch, heads, headdim, dstate;
+    long long seqlen;
+    int in_dtype, out_dtype;
+    const void *x, *dt;
+    const float *A;
+    const void *B, *C;
+    const float *D, *dt_bias;
+    int dt_softplus;
+    const float *h0;
+    void *y;
+    float *h_last;
+} ss_ssd_args;
+
+int ss_ssd_fwd(ss_ctx *ctx, const ss_ssd_args *args, ss_stream_t stream);
+
+/*
  * Causal depthwise 1D convolution: the Mamba block's convolution in front of
  * the selective scan ("Mamba: Linear-Time Sequence Modeling with Selective
  * State Spaces", section "Key terms", the Mamba block; soft186.com,

@@ -55,6 +55,15 @@ class ScanBwdArgs(ctypes.Structure):
                 ("dB", _vp), ("dC", _vp), ("dD", _vp), ("ddelta_bias", _vp), ("dh0", _vp)]
 
 
+class SsdArgs(ctypes.Structure):
+    """Mirror of ss_ssd_args."""
+    _fields_ = [("batch", ctypes.c_int), ("heads", ctypes.c_int), ("headdim", ctypes.c_int),
+                ("dstate", ctypes.c_int), ("seqlen", ctypes.c_longlong),
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("x", _vp),
+                ("dt", _vp), ("A", _vp), ("B", _vp), ("C", _vp), ("D", _vp), ("dt_bias", _vp),
+                ("dt_softplus", ctypes.c_int), ("h0", _vp), ("y", _vp), ("h_last", _vp)]
+
+
 class Conv1dArgs(ctypes.Structure):
     """Mirror of ss_conv1d_args."""
     _fields_ = [("batch", ctypes.c_int), ("dim", ctypes.c_int), ("width", ctypes.c_int),
@@ -97,6 +106,7 @@ def lib():
             L.ss_state_update.argtypes = [_vp, ctypes.POINTER(UpdateArgs), _vp]
             L.ss_conv1d_fwd.argtypes = [_vp, ctypes.POINTER(Conv1dArgs), _vp]
             L.ss_scan_bwd.argtypes = [_vp, ctypes.POINTER(ScanBwdArgs), _vp]
+            L.ss_ssd_fwd.argtypes = [_vp, ctypes.POINTER(SsdArgs), _vp]
             L.ss_conv1d_update.argtypes = [_vp, ctypes.POINTER(Conv1dUpdateArgs), _vp]
             L.ss_get_device_error.argtypes = [_vp, _vp]
             L.ss_status_string.argtypes = [ctypes.c_int]
@@ -370,6 +380,43 @@ def ss_scan_bwd(u, delta, A, B, C, dy, D=None, delta_bias=None, z=None, delta_so
     return g
 
 
+def ss_ssd_fwd(x, dt, A, B, C, D=None, dt_bias=None, dt_softplus=True, h0=None, y=None,
+               h_last=None, out_dtype=None, return_last_state=True, ctx: Context | None = None,
+               stream=None):
+    """Mamba-2 SSD forward on the GPU (chunked, tensor-core products).
+
+    x (batch, L, heads, headdim) bfloat16; dt (batch, L, heads) bfloat16;
+    A (heads,) float32; B, C (batch, L, dstate) bfloat16; D, dt_bias (heads,)
+    float32 or None; h0 (batch, heads, headdim, dstate) float32 or None.
+    Returns (y, h_last); y defaults to float32."""
+    import torch
+    _need(x, "x")
+    batch, L, H, P = x.shape
+    N = B.shape[2]
+    dev = x.device
+    _need(dt, "dt", (batch, L, H), x.dtype, dev)
+    _need(A, "A", (H,), torch.float32, dev)
+    _need(B, "B", (batch, L, N), x.dtype, dev)
+    _need(C, "C", (batch, L, N), x.dtype, dev)
+    for t, name in ((D, "D"), (dt_bias, "dt_bias")):
+        if t is not None:
+            _need(t, name, (H,), torch.float32, dev)
+    if h0 is not None:
+        _need(h0, "h0", (batch, H, P, N), torch.float32, dev)
+    if y is None:
+        y = torch.empty((batch, L, H, P), dtype=out_dtype or torch.float32, device=dev)
+    _need(y, "y", (batch, L, H, P), None, dev)
+    if h_last is None and return_last_state:
+        h_last = torch.empty((batch, H, P, N), dtype=torch.float32, device=dev)
+    if h_last is not None:
+        _need(h_last, "h_last", (batch, H, P, N), torch.float32, dev)
+    a = SsdArgs(batch, H, P, N, L, _dtype_code(x), _dtype_code(y), _p(x), _p(dt), _p(A), _p(B),
+                _p(C), _p(D), _p(dt_bias), int(bool(dt_softplus)), _p(h0), _p(y), _p(h_last))
+    ctx = ctx or default_context(dev.index if dev.index is not None else 0)
+    _check(lib().ss_ssd_fwd(ctx.handle, ctypes.byref(a), _stream_ptr(stream, dev)), "ss_ssd_fwd")
+    return y, h_last
+
+
 def ss_conv1d_fwd(x, weight, bias=None, init_state=None, silu=False, out=None,
                   final_state=None, out_dtype=None, return_final_state=True,
                   ctx: Context | None = None, stream=None):
@@ -431,6 +478,8 @@ def ss_conv1d_update(state, x, weight, bias=None, silu=False, out=None, out_dtyp
     return out
 
 
-__all__ = ["ss_scan_fwd", "ss_scan_bwd", "ss_state_update", "ss_conv1d_fwd", "ss_conv1d_update",
+__all__ = ["ss_scan_fwd", "ss_scan_bwd", "ss_ssd_fwd", "ss_state_update", "ss_conv1d_fwd",
+           "ss_conv1d_update",
            "PreparedScan", "Context", "SSError", "lib", "status_string",
-           "ScanArgs", "UpdateArgs", "ScanBwdArgs", "Conv1dArgs", "Conv1dUpdateArgs", "LIB_PATH"]
+           "ScanArgs", "UpdateArgs", "ScanBwdArgs", "SsdArgs", "Conv1dArgs", "Conv1dUpdateArgs",
+           "LIB_PATH"]

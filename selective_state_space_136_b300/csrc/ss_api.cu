@@ -405,6 +405,43 @@ int ss_scan_bwd(ss_ctx *ctx, const ss_scan_bwd_args *a, ss_stream_t stream) {
     return rc;
 }
 
+int ss_ssd_fwd(ss_ctx *ctx, const ss_ssd_args *a, ss_stream_t stream) {
+    if (!ctx || !a) return SS_ERR_INVALID_ARG;
+    if (a->batch < 1 || a->heads < 1 || a->headdim < 1 || a->dstate < 1 || a->seqlen < 1)
+        return SS_ERR_INVALID_ARG;
+    if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return SS_ERR_INVALID_ARG;
+    if (!a->x || !a->dt || !a->A || !a->B || !a->C || !a->y) return SS_ERR_INVALID_ARG;
+    const void *ptrs[] = {a->x, a->dt, a->A, a->B, a->C, a->D, a->dt_bias, a->h0, a->y, a->h_last};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return SS_ERR_INVALID_ARG;
+    if ((long long)a->batch * a->heads > (1LL << 30) || a->seqlen >= (1LL << 35))
+        return SS_ERR_INVALID_ARG;
+    const size_t esz = a->in_dtype == SS_BF16 ? 2 : 4, osz = a->out_dtype == SS_BF16 ? 2 : 4;
+    const size_t BL = (size_t)a->batch * (size_t)a->seqlen;
+    const size_t nx = BL * a->heads * a->headdim;
+    const size_t nst = (size_t)a->batch * a->heads * a->headdim * a->dstate * 4;
+    const Span y = span(a->y, nx * osz), hl = span(a->h_last, a->h_last ? nst : 0);
+    const Span ins[] = {span(a->x, nx * esz), span(a->dt, BL * a->heads * esz),
+                        span(a->A, (size_t)a->heads * 4), span(a->B, BL * a->dstate * esz),
+                        span(a->C, BL * a->dstate * esz),
+                        span(a->D, a->D ? (size_t)a->heads * 4 : 0),
+                        span(a->dt_bias, a->dt_bias ? (size_t)a->heads * 4 : 0)};
+    for (const Span &s : ins)
+        if (overlaps(y, s) || overlaps(hl, s)) return SS_ERR_INVALID_ARG;
+    if (overlaps(y, span(a->h0, a->h0 ? nst : 0)) || overlaps(y, hl)) return SS_ERR_INVALID_ARG;
+    if (a->h0 && a->h_last && a->h0 != a->h_last && overlaps(span(a->h0, nst), hl))
+        return SS_ERR_INVALID_ARG;
+    ssh::SsdParams p{a->batch, a->heads, a->headdim, a->dstate, a->seqlen, a->in_dtype,
+                     a->out_dtype, a->x, a->dt, a->A, a->B, a->C, a->D, a->dt_bias,
+                     a->dt_softplus, a->h0, a->y, a->h_last};
+    if (!ssh::ssd_supported(p)) return SS_ERR_UNSUPPORTED;
+    if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
+    const int rc = ssh::launch_ssd(p, reinterpret_cast<cudaStream_t>(stream));
+    ctx->last_variant = 0;
+    ctx->last_launches = rc == SS_OK ? 1 : 0;
+    return rc;
+}
+
 int ss_conv1d_fwd(ss_ctx *ctx, const ss_conv1d_args *a, ss_stream_t stream) {
     if (!ctx || !a) return SS_ERR_INVALID_ARG;
     if (a->batch < 1 || a->dim < 1 || a->seqlen < 0) return SS_ERR_INVALID_ARG;

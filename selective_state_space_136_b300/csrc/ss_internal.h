@@ -114,6 +114,23 @@ size_t bwd_ckpt_bytes(const BwdParams &p);
 bool bwd_supported(const BwdParams &p);
 int launch_bwd(const BwdParams &p, cudaStream_t st);
 
+// Mamba-2 SSD forward (ss_ssd.cu)
+struct SsdParams {
+    int batch, heads, headdim, dstate;
+    long long seqlen;
+    int in_dtype, out_dtype;
+    const void *x, *dt;
+    const float *A;
+    const void *B, *C;
+    const float *D, *dt_bias;
+    int softplus;
+    const float *h0;
+    void *y;
+    float *h_last;
+};
+bool ssd_supported(const SsdParams &p);
+int launch_ssd(const SsdParams &p, cudaStream_t st);
+
 // causal depthwise conv1d (ss_conv.cu)
 struct ConvParams {
     int batch, dim, width;

@@ -35,7 +35,7 @@ def test_struct_layout_matches_binding(built, tmp_path):
     """ctypes mirrors of the argument structs have the C layout."""
     import selective_state_space_136_b300 as ss
     structs = {"ss_scan_args": ss.ScanArgs, "ss_update_args": ss.UpdateArgs,
-               "ss_scan_bwd_args": ss.ScanBwdArgs,
+               "ss_scan_bwd_args": ss.ScanBwdArgs, "ss_ssd_args": ss.SsdArgs,
                "ss_conv1d_args": ss.Conv1dArgs, "ss_conv1d_update_args": ss.Conv1dUpdateArgs}
     prog = tmp_path / "layout.c"
     body = ['#include <stdio.h>', '#include <stddef.h>', '#include "ss_scan.h"', "int main(void){"]
@@ -68,6 +68,7 @@ def test_host_validation_without_gpu(built):
     assert L.ss_state_update(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_conv1d_fwd(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_scan_bwd(None, None, None) == ss.SS_ERR_INVALID_ARG
+    assert L.ss_ssd_fwd(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_conv1d_update(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_set_option(None, 0, 0) == ss.SS_ERR_INVALID_ARG
     assert L.ss_destroy(None) == ss.SS_OK
