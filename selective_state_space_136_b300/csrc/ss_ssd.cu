@@ -58,13 +58,6 @@ __device__ __forceinline__ float bf16_round(float v) {
     return __bfloat162float(__float2bfloat16_rn(v));
 }
 
-// 8 consecutive inputs (16-byte aligned) widened to fp32
-__device__ __forceinline__ void load_vec8(const uint16_t *p, float *v) {
-    const uint4 t = *reinterpret_cast<const uint4 *>(p);
-    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) v[2 * k] = bf16lo(w[k]), v[2 * k + 1] = bf16hi(w[k]);
-}
 __device__ __forceinline__ void store_pair(float *p, float a, float b) {
     *reinterpret_cast<float2 *>(p) = make_float2(a, b);
 }
@@ -167,30 +160,22 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
     for (int c = 0; c < n_chunks; ++c) {
         const long long l0 = (long long)c * kQ;
         __syncthreads();  // the previous chunk is done with X, Xs, B, C, dt, cum
-        // ---- load the chunk: x (Q x P), B and C (Q x N), dt
+        // ---- load the chunk: x (Q x P), B and C (Q x N) straight into shared
+        // memory by asynchronous 16-byte copies (all in flight at once)
         for (int i = tid; i < kQ * kP / 8; i += 128) {
             const int t = i / (kP / 8), c8 = (i % (kP / 8)) * 8;
             const Tin *src = static_cast<const Tin *>(p.x) + ((long long)b * L + l0 + t) * xs_t +
                              (long long)h * kP + c8;
-            float v[8];
-            load_vec8(src, v);
-            uint4 w;
-            w.x = pack_bf16(v[0], v[1]), w.y = pack_bf16(v[2], v[3]);
-            w.z = pack_bf16(v[4], v[5]), w.w = pack_bf16(v[6], v[7]);
-            *reinterpret_cast<uint4 *>(&sm.X[t][c8]) = w;
+            cp_async16(&sm.X[t][c8], src, 16);
         }
         for (int i = tid; i < 2 * kQ * N / 8; i += 128) {
             const int which = i / (kQ * N / 8), j = i % (kQ * N / 8);
             const int t = j / (N / 8), c8 = (j % (N / 8)) * 8;
             const Tin *src = static_cast<const Tin *>(which ? p.C : p.B) +
                              ((long long)b * L + l0 + t) * N + c8;
-            float v[8];
-            load_vec8(src, v);
-            uint4 w;
-            w.x = pack_bf16(v[0], v[1]), w.y = pack_bf16(v[2], v[3]);
-            w.z = pack_bf16(v[4], v[5]), w.w = pack_bf16(v[6], v[7]);
-            *reinterpret_cast<uint4 *>(which ? &sm.Cm[t][c8] : &sm.Bm[t][c8]) = w;
+            cp_async16(which ? &sm.Cm[t][c8] : &sm.Bm[t][c8], src, 16);
         }
+        cp_async_commit();
         if (warp == 0) {
             // dt_t and the inclusive prefix sum of dt_t a over the chunk (2 steps per lane)
             float d2[2], s2[2];
@@ -213,6 +198,7 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
             sm.cum[2 * lane] = before + s2[0];
             sm.cum[2 * lane + 1] = before + s2[0] + s2[1];
         }
+        cp_async_wait_all();
         __syncthreads();
 
         // ---- G = C B^T for rows t in [16 warp, 16 warp + 16), all s
