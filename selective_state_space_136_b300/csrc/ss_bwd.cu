@@ -29,6 +29,10 @@ namespace {
 
 using namespace ssk;
 
+#ifndef SS_BWD_PACKED
+#define SS_BWD_PACKED 1  // packed fp32x2 kernel for even N
+#endif
+
 constexpr int kTL = 16;   // steps per tile (checkpoint spacing)
 constexpr int kHalf = 8;  // steps recomputed into shared memory at a time
 
@@ -295,10 +299,283 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ssh::BwdParams p) {
     }
 }
 
+// The same algorithm with the states of a row taken two at a time in packed
+// fp32x2 arithmetic (N even), the reverse walk of a half tile kept rolled (a
+// small loop body), and the recomputed states stored as pairs.
+template <int N>
+struct BwdSmem2 {
+    float bc[kTL][2 * N];            // B (n < N), C (n >= N) of the tile, fp32
+    float2 S[kHalf][N / 2][32];      // recomputed states, pairs (n, n+1) per lane
+    float in[5][kTL][32];            // dt, u, sigmoid(x), z, dy per lane
+    float out[3][kTL][32];           // du, ddelta, dz per lane
+};
+
 template <typename Tin, int N>
-int bwd_n(const ssh::BwdParams &p, cudaStream_t st) {
-    const int smem = (int)sizeof(BwdSmem<N>);
-    auto kern = scan_bwd_kernel<Tin, N>;
+__global__ void __launch_bounds__(32) scan_bwd2_kernel(const ssh::BwdParams p) {
+    constexpr int NP = N / 2;
+    constexpr unsigned FULL = 0xffffffffu;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    BwdSmem2<N> &sm = *reinterpret_cast<BwdSmem2<N> *>(smem_raw);
+    const int lane = threadIdx.x;
+    const int rb_per_batch = (p.dim + 31) / 32;
+    const int b = blockIdx.x / rb_per_batch, blk = blockIdx.x % rb_per_batch;
+    const int d = blk * 32 + lane;
+    const bool row_ok = d < p.dim;
+    const int dc = row_ok ? d : p.dim - 1;
+    const long long row = (long long)b * p.dim + dc;
+    const long long L = p.seqlen;
+    const int K = (int)(L / kTL);
+
+    f2 A2[NP], Ar[NP];  // A log2(e) and A, pairs
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        const float a0 = p.A[(long long)dc * N + 2 * j], a1 = p.A[(long long)dc * N + 2 * j + 1];
+        A2[j] = mk2(a0 * kLog2e, a1 * kLog2e);
+        Ar[j] = mk2(a0, a1);
+    }
+    const float bias = p.bias ? p.bias[dc] : 0.f;
+    const float Dd = p.D ? p.D[dc] : 0.f;
+    const Tin *gu = static_cast<const Tin *>(p.u) + row * L;
+    const Tin *gd = static_cast<const Tin *>(p.delta) + row * L;
+    const Tin *gz = p.z ? static_cast<const Tin *>(p.z) + row * L : nullptr;
+    float *ck = p.ckpt + ((long long)blockIdx.x * 32 + lane) * (long long)K * N;
+
+    auto bc_load = [&](long long l0) {
+        __syncwarp();
+        if (lane < 2 * N) {
+            const int n = lane % N;
+            const Tin *src = static_cast<const Tin *>(lane < N ? p.B : p.C) +
+                             ((long long)b * N + n) * L + l0;
+            float v[kTL];
+            load_tile(src, v);
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) sm.bc[t][lane] = v[t];
+        }
+        __syncwarp();
+    };
+    auto Bpair = [&](int t, int j) {
+        const float2 v = *reinterpret_cast<const float2 *>(&sm.bc[t][2 * j]);
+        return mk2(v.x, v.y);
+    };
+    auto Cpair = [&](int t, int j) {
+        const float2 v = *reinterpret_cast<const float2 *>(&sm.bc[t][N + 2 * j]);
+        return mk2(v.x, v.y);
+    };
+    auto fwd_step = [&](f2 *h, float dt, float du, int t) {
+        const f2 dd = mk2(dt, dt), uu = mk2(du, du);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const f2 tt = fmul2(dd, A2[j]);
+            h[j] = ffma2(mk2(ex2(tt.x), ex2(tt.y)), h[j], fmul2(uu, Bpair(t, j)));
+        }
+    };
+
+    // ---- forward sweep: the state entering every tile
+    {
+        f2 h[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j)
+            h[j] = p.h0 ? mk2(p.h0[row * N + 2 * j], p.h0[row * N + 2 * j + 1]) : mk2(0.f, 0.f);
+        for (int k = 0; k < K; ++k) {
+            const long long l0 = (long long)k * kTL;
+#pragma unroll
+            for (int j = 0; j < NP; ++j)
+                *reinterpret_cast<float2 *>(ck + (long long)k * N + 2 * j) = make_float2(h[j].x, h[j].y);
+            bc_load(l0);
+            float uv[kTL], dl[kTL];
+            load_tile(gu + l0, uv);
+            load_tile(gd + l0, dl);
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) {
+                const float x = dl[t] + bias;
+                const float dt = p.softplus ? softplus1(x) : x;
+                fwd_step(h, dt, dt * uv[t], t);
+            }
+        }
+    }
+
+    // ---- reverse sweep
+    f2 g[NP], gA[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        g[j] = (row_ok && p.dh_last) ? mk2(p.dh_last[row * N + 2 * j], p.dh_last[row * N + 2 * j + 1])
+                                     : mk2(0.f, 0.f);
+        gA[j] = mk2(0.f, 0.f);
+    }
+    float gD = 0.f, gbias = 0.f;
+    for (int k = K - 1; k >= 0; --k) {
+        const long long l0 = (long long)k * kTL;
+        bc_load(l0);
+        {
+            float uv[kTL], dl[kTL], v[kTL];
+            load_tile(gu + l0, uv);
+            load_tile(gd + l0, dl);
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) {
+                const float x = dl[t] + bias;
+                sm.in[0][t][lane] = p.softplus ? softplus1(x) : x;
+                sm.in[1][t][lane] = uv[t];
+                sm.in[2][t][lane] = __fdividef(1.f, 1.f + ex2(-x * kLog2e));
+            }
+            if (gz) {
+                load_tile(gz + l0, v);
+#pragma unroll
+                for (int t = 0; t < kTL; ++t) sm.in[3][t][lane] = v[t];
+            }
+            load_tile(p.dy + row * L + l0, v);
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) sm.in[4][t][lane] = row_ok ? v[t] : 0.f;
+        }
+        __syncwarp();
+        f2 hc[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const float2 v = *reinterpret_cast<const float2 *>(ck + (long long)k * N + 2 * j);
+            hc[j] = mk2(v.x, v.y);
+        }
+
+#pragma unroll 1
+        for (int half = 1; half >= 0; --half) {
+            const int t0 = half * kHalf;
+            f2 hp[NP];
+#pragma unroll
+            for (int j = 0; j < NP; ++j) hp[j] = hc[j];
+            if (half == 1) {
+#pragma unroll 1
+                for (int t = 0; t < kHalf; ++t) {
+                    const float dtt = sm.in[0][t][lane];
+                    fwd_step(hp, dtt, dtt * sm.in[1][t][lane], t);
+                }
+            }
+            {
+                f2 hh[NP];
+#pragma unroll
+                for (int j = 0; j < NP; ++j) hh[j] = hp[j];
+#pragma unroll 1
+                for (int t = 0; t < kHalf; ++t) {
+                    const float dtt = sm.in[0][t0 + t][lane];
+                    fwd_step(hh, dtt, dtt * sm.in[1][t0 + t][lane], t0 + t);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) sm.S[t][j][lane] = make_float2(hh[j].x, hh[j].y);
+                }
+            }
+            __syncwarp();
+            f2 hcur[NP];
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const float2 v = sm.S[kHalf - 1][j][lane];
+                hcur[j] = mk2(v.x, v.y);
+            }
+#pragma unroll 1
+            for (int t = kHalf - 1; t >= 0; --t) {
+                const int tt = t0 + t;
+                const float dtt = sm.in[0][tt][lane], u = sm.in[1][tt][lane];
+                const float dyt = sm.in[4][tt][lane];
+                f2 hprev[NP];
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const float2 v = t > 0 ? sm.S[t - 1][j][lane] : make_float2(hp[j].x, hp[j].y);
+                    hprev[j] = mk2(v.x, v.y);
+                }
+                f2 s2 = mk2(Dd * u, 0.f);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) s2 = ffma2(Cpair(tt, j), hcur[j], s2);
+                const float s = s2.x + s2.y;
+                float gs = dyt;
+                if (gz) {
+                    const float zz = sm.in[3][tt][lane];
+                    const float sg = __fdividef(1.f, 1.f + ex2(-zz * kLog2e));
+                    sm.out[2][tt][lane] = dyt * s * sg * fmaf(zz, 1.f - sg, 1.f);
+                    gs = dyt * zz * sg;
+                }
+                gD = fmaf(gs, u, gD);
+                const f2 gs2 = mk2(gs, gs), dd = mk2(dtt, dtt), uu = mk2(u, u);
+                f2 gu2 = mk2(gs * Dd, 0.f), gdt2 = mk2(0.f, 0.f);
+                float v[2 * N];  // this row's dB (n < N) and dC terms of the step
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const f2 Bp = Bpair(tt, j), Cp = Cpair(tt, j);
+                    const f2 tq = fmul2(dd, A2[j]);
+                    const f2 e = mk2(ex2(tq.x), ex2(tq.y));
+                    g[j] = ffma2(gs2, Cp, g[j]);
+                    const f2 vc = fmul2(gs2, hcur[j]);
+                    const f2 gdu = fmul2(g[j], dd);
+                    const f2 vb = fmul2(gdu, uu);
+                    v[2 * j] = vb.x, v[2 * j + 1] = vb.y;
+                    v[N + 2 * j] = vc.x, v[N + 2 * j + 1] = vc.y;
+                    gu2 = ffma2(gdu, Bp, gu2);
+                    const f2 ehp = fmul2(e, hprev[j]);
+                    gdt2 = ffma2(g[j], ffma2(Ar[j], ehp, fmul2(Bp, uu)), gdt2);
+                    gA[j] = ffma2(gdu, ehp, gA[j]);
+                    g[j] = fmul2(g[j], e);
+                    hcur[j] = hprev[j];
+                }
+                const float gdt = gdt2.x + gdt2.y;
+                const float gx = p.softplus ? gdt * sm.in[2][tt][lane] : gdt;
+                gbias += gx;
+                sm.out[0][tt][lane] = gu2.x + gu2.y;
+                sm.out[1][tt][lane] = gx;
+                // dB and dC of the step summed over the warp's rows (shuffle
+                // reduce-scatter; lane L ends with value L % 2N)
+#pragma unroll
+                for (int w = 16; w >= 2 * N; w >>= 1)
+#pragma unroll
+                    for (int i = 0; i < 2 * N; ++i) v[i] += __shfl_xor_sync(FULL, v[i], w);
+#pragma unroll
+                for (int w = (2 * N < 32 ? N : 16); w >= 1; w >>= 1) {
+                    const bool upper = (lane & w) != 0;
+#pragma unroll
+                    for (int i = 0; i < w; ++i) {
+                        const float send = upper ? v[i] : v[i + w];
+                        const float keep = upper ? v[i + w] : v[i];
+                        v[i] = keep + __shfl_xor_sync(FULL, send, w);
+                    }
+                }
+                if (lane < 2 * N) {
+                    const int n = lane % N;
+                    float *dst = (lane < N ? p.dB : p.dC) + ((long long)b * N + n) * L + l0 + tt;
+                    atomicAdd(dst, v[0]);
+                }
+            }
+            __syncwarp();
+        }
+        __syncwarp();
+        if (row_ok) {
+            float o[kTL];
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) o[t] = sm.out[0][t][lane];
+            store_tile16(p.du + row * L + l0, o);
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) o[t] = sm.out[1][t][lane];
+            store_tile16(p.ddelta + row * L + l0, o);
+            if (p.dz) {
+#pragma unroll
+                for (int t = 0; t < kTL; ++t) o[t] = sm.out[2][t][lane];
+                store_tile16(p.dz + row * L + l0, o);
+            }
+        }
+    }
+    if (row_ok) {
+        if (p.dh0) {
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                p.dh0[row * N + 2 * j] = g[j].x;
+                p.dh0[row * N + 2 * j + 1] = g[j].y;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            atomicAdd(p.dA + (long long)dc * N + 2 * j, gA[j].x);
+            atomicAdd(p.dA + (long long)dc * N + 2 * j + 1, gA[j].y);
+        }
+        if (p.dD) atomicAdd(p.dD + dc, gD);
+        if (p.dbias) atomicAdd(p.dbias + dc, gbias);
+    }
+}
+
+template <typename Tin, int N, typename Smem, typename Kern>
+int bwd_launch(Kern kern, const ssh::BwdParams &p, cudaStream_t st) {
+    const int smem = (int)sizeof(Smem);
     static bool attr_done[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
@@ -311,6 +588,14 @@ int bwd_n(const ssh::BwdParams &p, cudaStream_t st) {
     const long long blocks = (long long)p.batch * ((p.dim + 31) / 32);
     kern<<<(unsigned)blocks, 32, smem, st>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+template <typename Tin, int N>
+int bwd_n(const ssh::BwdParams &p, cudaStream_t st) {
+    if constexpr (SS_BWD_PACKED && N % 2 == 0)
+        return bwd_launch<Tin, N, BwdSmem2<N>>(scan_bwd2_kernel<Tin, N>, p, st);
+    else
+        return bwd_launch<Tin, N, BwdSmem<N>>(scan_bwd_kernel<Tin, N>, p, st);
 }
 
 template <typename Tin>
