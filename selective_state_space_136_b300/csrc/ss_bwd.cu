@@ -305,13 +305,14 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ssh::BwdParams p) {
 template <int N>
 struct BwdSmem2 {
     float bc[kTL][2 * N];            // B (n < N), C (n >= N) of the tile, fp32
-    float2 S[kHalf][N / 2][32];      // recomputed states, pairs (n, n+1) per lane
-    float in[5][kTL][32];            // dt, u, sigmoid(x), z, dy per lane
-    float out[3][kTL][32];           // du, ddelta, dz per lane
+    float2 S[kHalf - 1][N / 2][32];  // recomputed states but the last, pairs (n, n+1) per lane
+    // per lane: dt, u, z, dy of each step; once step t has been walked back its
+    // slots take ddelta, du and dz (nothing reads dt, u or z of step t after that)
+    float io[4][kTL][32];
 };
 
 template <typename Tin, int N>
-__global__ void __launch_bounds__(32) scan_bwd2_kernel(const ssh::BwdParams p) {
+__global__ void __launch_bounds__(32, 9) scan_bwd2_kernel(const ssh::BwdParams p) {
     constexpr int NP = N / 2;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -326,13 +327,10 @@ __global__ void __launch_bounds__(32) scan_bwd2_kernel(const ssh::BwdParams p) {
     const long long L = p.seqlen;
     const int K = (int)(L / kTL);
 
-    f2 A2[NP], Ar[NP];  // A log2(e) and A, pairs
+    f2 Ar[NP];  // A, pairs; exp(dt a) is taken as ex2((dt log2 e) a)
 #pragma unroll
-    for (int j = 0; j < NP; ++j) {
-        const float a0 = p.A[(long long)dc * N + 2 * j], a1 = p.A[(long long)dc * N + 2 * j + 1];
-        A2[j] = mk2(a0 * kLog2e, a1 * kLog2e);
-        Ar[j] = mk2(a0, a1);
-    }
+    for (int j = 0; j < NP; ++j)
+        Ar[j] = mk2(p.A[(long long)dc * N + 2 * j], p.A[(long long)dc * N + 2 * j + 1]);
     const float bias = p.bias ? p.bias[dc] : 0.f;
     const float Dd = p.D ? p.D[dc] : 0.f;
     const Tin *gu = static_cast<const Tin *>(p.u) + row * L;
@@ -362,10 +360,11 @@ __global__ void __launch_bounds__(32) scan_bwd2_kernel(const ssh::BwdParams p) {
         return mk2(v.x, v.y);
     };
     auto fwd_step = [&](f2 *h, float dt, float du, int t) {
-        const f2 dd = mk2(dt, dt), uu = mk2(du, du);
+        const float dl = dt * kLog2e;
+        const f2 dd = mk2(dl, dl), uu = mk2(du, du);
 #pragma unroll
         for (int j = 0; j < NP; ++j) {
-            const f2 tt = fmul2(dd, A2[j]);
+            const f2 tt = fmul2(dd, Ar[j]);
             h[j] = ffma2(mk2(ex2(tt.x), ex2(tt.y)), h[j], fmul2(uu, Bpair(t, j)));
         }
     };
@@ -413,18 +412,17 @@ __global__ void __launch_bounds__(32) scan_bwd2_kernel(const ssh::BwdParams p) {
 #pragma unroll
             for (int t = 0; t < kTL; ++t) {
                 const float x = dl[t] + bias;
-                sm.in[0][t][lane] = p.softplus ? softplus1(x) : x;
-                sm.in[1][t][lane] = uv[t];
-                sm.in[2][t][lane] = __fdividef(1.f, 1.f + ex2(-x * kLog2e));
+                sm.io[0][t][lane] = p.softplus ? softplus1(x) : x;
+                sm.io[1][t][lane] = uv[t];
             }
             if (gz) {
                 load_tile(gz + l0, v);
 #pragma unroll
-                for (int t = 0; t < kTL; ++t) sm.in[3][t][lane] = v[t];
+                for (int t = 0; t < kTL; ++t) sm.io[2][t][lane] = v[t];
             }
             load_tile(p.dy + row * L + l0, v);
 #pragma unroll
-            for (int t = 0; t < kTL; ++t) sm.in[4][t][lane] = row_ok ? v[t] : 0.f;
+            for (int t = 0; t < kTL; ++t) sm.io[3][t][lane] = row_ok ? v[t] : 0.f;
         }
         __syncwarp();
         f2 hc[NP];
@@ -443,34 +441,28 @@ __global__ void __launch_bounds__(32) scan_bwd2_kernel(const ssh::BwdParams p) {
             if (half == 1) {
 #pragma unroll 1
                 for (int t = 0; t < kHalf; ++t) {
-                    const float dtt = sm.in[0][t][lane];
-                    fwd_step(hp, dtt, dtt * sm.in[1][t][lane], t);
+                    const float dtt = sm.io[0][t][lane];
+                    fwd_step(hp, dtt, dtt * sm.io[1][t][lane], t);
                 }
             }
-            {
-                f2 hh[NP];
+            f2 hcur[NP];  // after the loop: the state after the half's last step
 #pragma unroll
-                for (int j = 0; j < NP; ++j) hh[j] = hp[j];
+            for (int j = 0; j < NP; ++j) hcur[j] = hp[j];
 #pragma unroll 1
-                for (int t = 0; t < kHalf; ++t) {
-                    const float dtt = sm.in[0][t0 + t][lane];
-                    fwd_step(hh, dtt, dtt * sm.in[1][t0 + t][lane], t0 + t);
+            for (int t = 0; t < kHalf; ++t) {
+                const float dtt = sm.io[0][t0 + t][lane];
+                fwd_step(hcur, dtt, dtt * sm.io[1][t0 + t][lane], t0 + t);
+                if (t < kHalf - 1) {
 #pragma unroll
-                    for (int j = 0; j < NP; ++j) sm.S[t][j][lane] = make_float2(hh[j].x, hh[j].y);
+                    for (int j = 0; j < NP; ++j) sm.S[t][j][lane] = make_float2(hcur[j].x, hcur[j].y);
                 }
             }
             __syncwarp();
-            f2 hcur[NP];
-#pragma unroll
-            for (int j = 0; j < NP; ++j) {
-                const float2 v = sm.S[kHalf - 1][j][lane];
-                hcur[j] = mk2(v.x, v.y);
-            }
 #pragma unroll 1
             for (int t = kHalf - 1; t >= 0; --t) {
                 const int tt = t0 + t;
-                const float dtt = sm.in[0][tt][lane], u = sm.in[1][tt][lane];
-                const float dyt = sm.in[4][tt][lane];
+                const float dtt = sm.io[0][tt][lane], u = sm.io[1][tt][lane];
+                const float dyt = sm.io[3][tt][lane];
                 f2 hprev[NP];
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
@@ -483,19 +475,20 @@ __global__ void __launch_bounds__(32) scan_bwd2_kernel(const ssh::BwdParams p) {
                 const float s = s2.x + s2.y;
                 float gs = dyt;
                 if (gz) {
-                    const float zz = sm.in[3][tt][lane];
+                    const float zz = sm.io[2][tt][lane];
                     const float sg = __fdividef(1.f, 1.f + ex2(-zz * kLog2e));
-                    sm.out[2][tt][lane] = dyt * s * sg * fmaf(zz, 1.f - sg, 1.f);
+                    sm.io[2][tt][lane] = dyt * s * sg * fmaf(zz, 1.f - sg, 1.f);
                     gs = dyt * zz * sg;
                 }
                 gD = fmaf(gs, u, gD);
-                const f2 gs2 = mk2(gs, gs), dd = mk2(dtt, dtt), uu = mk2(u, u);
+                const float dl = dtt * kLog2e;
+                const f2 gs2 = mk2(gs, gs), dd = mk2(dtt, dtt), dd2 = mk2(dl, dl), uu = mk2(u, u);
                 f2 gu2 = mk2(gs * Dd, 0.f), gdt2 = mk2(0.f, 0.f);
                 float v[2 * N];  // this row's dB (n < N) and dC terms of the step
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
                     const f2 Bp = Bpair(tt, j), Cp = Cpair(tt, j);
-                    const f2 tq = fmul2(dd, A2[j]);
+                    const f2 tq = fmul2(dd2, Ar[j]);
                     const f2 e = mk2(ex2(tq.x), ex2(tq.y));
                     g[j] = ffma2(gs2, Cp, g[j]);
                     const f2 vc = fmul2(gs2, hcur[j]);
@@ -511,10 +504,11 @@ __global__ void __launch_bounds__(32) scan_bwd2_kernel(const ssh::BwdParams p) {
                     hcur[j] = hprev[j];
                 }
                 const float gdt = gdt2.x + gdt2.y;
-                const float gx = p.softplus ? gdt * sm.in[2][tt][lane] : gdt;
+                // softplus'(x) = sigmoid(x) = 1 - exp(-softplus(x))
+                const float gx = p.softplus ? gdt * -expm1f(-dtt) : gdt;
                 gbias += gx;
-                sm.out[0][tt][lane] = gu2.x + gu2.y;
-                sm.out[1][tt][lane] = gx;
+                sm.io[1][tt][lane] = gu2.x + gu2.y;
+                sm.io[0][tt][lane] = gx;
                 // dB and dC of the step summed over the warp's rows (shuffle
                 // reduce-scatter; lane L ends with value L % 2N)
 #pragma unroll
@@ -543,14 +537,14 @@ __global__ void __launch_bounds__(32) scan_bwd2_kernel(const ssh::BwdParams p) {
         if (row_ok) {
             float o[kTL];
 #pragma unroll
-            for (int t = 0; t < kTL; ++t) o[t] = sm.out[0][t][lane];
+            for (int t = 0; t < kTL; ++t) o[t] = sm.io[1][t][lane];
             store_tile16(p.du + row * L + l0, o);
 #pragma unroll
-            for (int t = 0; t < kTL; ++t) o[t] = sm.out[1][t][lane];
+            for (int t = 0; t < kTL; ++t) o[t] = sm.io[0][t][lane];
             store_tile16(p.ddelta + row * L + l0, o);
             if (p.dz) {
 #pragma unroll
-                for (int t = 0; t < kTL; ++t) o[t] = sm.out[2][t][lane];
+                for (int t = 0; t < kTL; ++t) o[t] = sm.io[2][t][lane];
                 store_tile16(p.dz + row * L + l0, o);
             }
         }
