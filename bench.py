@@ -200,7 +200,7 @@ def probe_alu(device):
     lib.ss_probe_alu.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(ctypes.c_double)]
     out = {}
-    for which, name in ((0, "ex2"), (1, "ffma"), (2, "ffma2")):
+    for which, name in ((0, "ex2"), (1, "ffma"), (2, "ffma2"), (3, "mixed")):
         r, g = ctypes.c_double(), ctypes.c_double()
         rc = lib.ss_probe_alu(which, device, ctypes.byref(r), ctypes.byref(g))
         out[name] = {"ops_per_s": r.value, "sm_ghz": g.value, "rc": rc}
@@ -660,6 +660,17 @@ def run_ours(args, rank, world, local):
     issue_floor_us = bdln * 5 / 32 / (4 * sms) / (MAX_SM_MHZ * 1e6) * 1e6
     issue_term = {"floor_us": issue_floor_us, "frac": issue_floor_us / (avg_launch_s * 1e6),
                   "note": "5 issue slots (4 FP32 + 1 MUFU) per 32 state elements, 4 schedulers/SM"}
+    # informative: the mixed probe runs ex2 and FFMA2 at the scan's ratio (one
+    # ex2 per four FMA lane-ops) on independent chains; its rate, scaled to the
+    # maximum clock, is what the two units deliver together
+    mixed_term = None
+    if probes and probes.get("mixed", {}).get("rc") == 0 and probes["mixed"]["sm_ghz"] > 0:
+        rate = probes["mixed"]["ops_per_s"] * (MAX_SM_MHZ * 1e-3) / probes["mixed"]["sm_ghz"]
+        per_clk = probes["mixed"]["ops_per_s"] / (sms * probes["mixed"]["sm_ghz"] * 1e9)
+        mixed_term = {"floor_us": bdln / rate * 1e6, "frac": bdln / rate / avg_launch_s,
+                      "elements_per_clk_per_sm": per_clk,
+                      "note": "state elements (1 ex2 + 4 FMA lane-ops) per second that the "
+                              "mixed probe sustains, at the maximum clock"}
     dt = terms[dominant]
     roofline = {"bound": "hbm" if dominant == "hbm" else "alu", "term": dominant,
                 "achieved": dt["achieved"], "peak": dt["peak"], "unit": dt["unit"],
@@ -670,7 +681,7 @@ def run_ours(args, rank, world, local):
                                "events on the launching stream, averaged over the timed steps",
                 "floor_us": max(t["floor_us"] for t in terms.values()),
                 "frac_of_floor": max(t["floor_us"] for t in terms.values()) / (avg_launch_s * 1e6),
-                "terms": terms, "issue_slots": issue_term, "peak_clock_mhz": MAX_SM_MHZ}
+                "terms": terms, "issue_slots": issue_term, "mixed_units": mixed_term, "peak_clock_mhz": MAX_SM_MHZ}
 
     cpu = None
     if not args.skip_cpu:

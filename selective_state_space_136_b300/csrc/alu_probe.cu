@@ -4,7 +4,9 @@
 // of the scan library.
 //
 // Each thread runs 8 independent dependency chains so the unit, not latency,
-// limits the rate. The kernel also records SM cycles (clock64) against the
+// limits the rate. The mixed probe runs the scan's own ratio, one ex2 to four
+// FMA lane-ops (two packed FFMA2), on independent chains: its rate shows
+// whether the two units overlap (time of the slower) or not (sum of both). The kernel also records SM cycles (clock64) against the
 // global nanosecond timer in one thread, which gives the SM clock the probe
 // actually ran at.
 #include <cuda_runtime.h>
@@ -35,9 +37,11 @@ __device__ __forceinline__ void ffma2(float &a0, float &a1, float b0, float b1, 
 template <int WHICH>
 __global__ void __launch_bounds__(256) probe_kernel(float *sink, int iters,
                                                     unsigned long long *clk) {
-    float a[8];
+    float a[8], c[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = 0.25f + 0.01f * i + 1e-6f * threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) c[i] = 0.5f + 0.01f * i + 1e-6f * threadIdx.x;
     uint64_t c0 = 0, t0 = 0;
     if (blockIdx.x == 0 && threadIdx.x == 0) c0 = clock64(), t0 = gtimer();
     for (int it = 0; it < iters; ++it) {
@@ -49,11 +53,20 @@ __global__ void __launch_bounds__(256) probe_kernel(float *sink, int iters,
             } else if constexpr (WHICH == 1) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) a[i] = fmaf(a[i], 0.9990234375f, 0.0009765625f);
-            } else {
+            } else if constexpr (WHICH == 2) {
 #pragma unroll
                 for (int i = 0; i < 8; i += 2)
                     ffma2(a[i], a[i + 1], 0.9990234375f, 0.9990234375f, 0.0009765625f,
                           0.0009765625f);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    a[i] = ex2(-a[i]);
+                    ffma2(c[(2 * i) % 16], c[(2 * i + 1) % 16], 0.9990234375f, 0.9990234375f,
+                          0.0009765625f, 0.0009765625f);
+                    ffma2(c[(2 * i + 2) % 16], c[(2 * i + 3) % 16], 0.9990234375f,
+                          0.9990234375f, 0.0009765625f, 0.0009765625f);
+                }
             }
         }
     }
@@ -64,6 +77,8 @@ __global__ void __launch_bounds__(256) probe_kernel(float *sink, int iters,
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) s += a[i];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s += c[i];
     if (s == 1234.5f) sink[threadIdx.x] = s;  // keeps the chains live
 }
 
@@ -71,10 +86,22 @@ __global__ void __launch_bounds__(256) probe_kernel(float *sink, int iters,
 
 extern "C" {
 
-// which: 0 = MUFU ex2, 1 = FFMA, 2 = packed FFMA2 (counted as 2 FMA each).
+// which: 0 = MUFU ex2, 1 = FFMA, 2 = packed FFMA2 (counted as 2 FMA each),
+// 3 = mixed (counted in ex2: each ex2 comes with four FMA lane-ops).
 // Writes the sustained rate in operations per second and the SM clock in GHz
 // seen by the probe. Returns 0 on success, the CUDA error code otherwise.
+int ss_probe_alu_occ(int which, int device, int warps_per_sm, double *ops_per_s,
+                     double *sm_ghz);
+
 int ss_probe_alu(int which, int device, double *ops_per_s, double *sm_ghz) {
+    return ss_probe_alu_occ(which, device, 64, ops_per_s, sm_ghz);
+}
+
+// The same probes with `warps_per_sm` warps resident per SM (blocks of up to
+// 256 threads, one wave): what a scheduler sustains with few warps to pick from.
+int ss_probe_alu_occ(int which, int device, int warps_per_sm, double *ops_per_s,
+                     double *sm_ghz) {
+    if (warps_per_sm < 1 || warps_per_sm > 64 || which < 0 || which > 3) return -1;
     cudaError_t e = cudaSetDevice(device);
     if (e != cudaSuccess) return (int)e;
     int sms = 0;
@@ -88,12 +115,14 @@ int ss_probe_alu(int which, int device, double *ops_per_s, double *sm_ghz) {
     cudaEvent_t a, b;
     cudaEventCreate(&a);
     cudaEventCreate(&b);
-    const int blocks = sms * 8, threads = 256;
-    const int iters = which == 0 ? 2048 : 8192;
+    const int threads = warps_per_sm >= 8 ? 256 : 32 * warps_per_sm;
+    const int blocks = sms * (warps_per_sm * 32 / threads);
+    const int iters = which == 0 || which == 3 ? 2048 : 8192;
     auto run = [&](int n) {
         if (which == 0) probe_kernel<0><<<blocks, threads, 0, st>>>(sink, n, clk);
         else if (which == 1) probe_kernel<1><<<blocks, threads, 0, st>>>(sink, n, clk);
-        else probe_kernel<2><<<blocks, threads, 0, st>>>(sink, n, clk);
+        else if (which == 2) probe_kernel<2><<<blocks, threads, 0, st>>>(sink, n, clk);
+        else probe_kernel<3><<<blocks, threads, 0, st>>>(sink, n, clk);
     };
     run(iters / 8);  // warm-up
     cudaEventRecord(a, st);
