@@ -17,9 +17,12 @@
 // run as bf16 mma.sync with fp32 accumulation; the carried state stays in fp32
 // accumulators and enters the C H_prev product as two bf16 terms (hi + lo).
 //
-// One CTA of 4 warps per (batch, head) walks the chunks in order; warp w
-// owns rows t in [16w, 16w+16) of the chunk products and state rows n in
-// [N/4 w, N/4 (w+1)) of the carried state.
+// One CTA of 4 warps per (batch, head, group of kPC channels) walks the
+// chunks in order; warp w owns rows t in [16w, 16w+16) of the chunk products
+// and state rows n in [N/4 w, N/4 (w+1)) of the carried state. Splitting a
+// head's channels over CTAs repeats the C B^T product in each but halves a
+// CTA's shared memory and work, so more CTAs run at once and the grid's last
+// wave is less empty.
 #include "ss_common.cuh"
 #include "ss_internal.h"
 
@@ -29,6 +32,11 @@ using namespace ssk;
 
 constexpr int kQ = 64;   // chunk length
 constexpr int kP = 64;   // head dimension
+#ifndef SS_SSD_PC
+#define SS_SSD_PC 32
+#endif
+constexpr int kPC = SS_SSD_PC;  // channels of the head per CTA
+static_assert(kP % kPC == 0 && kPC % 16 == 0, "channel groups of whole 16-column tiles");
 constexpr int kPad = 8;  // bf16 padding per smem row (rows 16 bytes apart in banks)
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -67,12 +75,12 @@ __device__ __forceinline__ void store_pair(uint16_t *p, float a, float b) {
 
 template <int N>
 struct SsdSmem {
-    uint16_t X[kQ][kP + kPad];     // x of the chunk, [t][p]
-    uint16_t Xs[kQ][kP + kPad];    // x scaled by exp(cum_last - cum_s) dt_s, [s][p]
+    uint16_t X[kQ][kPC + kPad];    // x of the chunk, [t][p]
+    uint16_t Xs[kQ][kPC + kPad];   // x scaled by exp(cum_last - cum_s) dt_s, [s][p]
     uint16_t Bm[kQ][N + kPad];     // B of the chunk, [s][n]
     uint16_t Cm[kQ][N + kPad];     // C of the chunk, [t][n]
-    uint16_t Hh[N][kP + kPad];     // carried state, high bf16 part, [n][p]
-    uint16_t Hl[N][kP + kPad];     // carried state, low bf16 part (H - hi), [n][p]
+    uint16_t Hh[N][kPC + kPad];    // carried state, high bf16 part, [n][p]
+    uint16_t Hl[N][kPC + kPad];    // carried state, low bf16 part (H - hi), [n][p]
     float dt[kQ];                  // dt_t of the chunk
     float cum[kQ];                 // cum_t
 };
@@ -118,7 +126,9 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
     constexpr int MT = NW / 16;  // 16-row tiles of the state per warp
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, tg = lane & 3;
-    const int b = blockIdx.x / p.heads, h = blockIdx.x % p.heads;
+    constexpr int NG = kP / kPC;  // channel groups per head
+    const int b = blockIdx.x / (p.heads * NG), h = (blockIdx.x / NG) % p.heads;
+    const int p0 = (blockIdx.x % NG) * kPC;  // first channel of this CTA
     const long long L = p.seqlen;
     const float a = p.A[h] * kLog2e;  // log2 units
     const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
@@ -126,16 +136,16 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
     const long long xs_t = (long long)p.heads * kP;  // x / y stride between steps
 
     // carried state of this warp's rows: Hacc[mt][pt][4] covers n = 16 mt + {g, g+8}
-    // (+ NW warp), p = 8 pt + 2 tg + {0, 1}
-    float Hacc[MT][kP / 8][4];
+    // (+ NW warp), p = p0 + 8 pt + 2 tg + {0, 1}
+    float Hacc[MT][kPC / 8][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int pt = 0; pt < kP / 8; ++pt)
+        for (int pt = 0; pt < kPC / 8; ++pt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int n = NW * warp + 16 * mt + g + (e >> 1) * 8;
-                const int pp = 8 * pt + 2 * tg + (e & 1);
+                const int pp = p0 + 8 * pt + 2 * tg + (e & 1);
                 Hacc[mt][pt][e] =
                     p.h0 ? p.h0[(((long long)b * p.heads + h) * kP + pp) * N + n] : 0.f;
             }
@@ -143,7 +153,7 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int pt = 0; pt < kP / 8; ++pt)
+            for (int pt = 0; pt < kPC / 8; ++pt)
 #pragma unroll
                 for (int e = 0; e < 4; e += 2) {
                     const int n = NW * warp + 16 * mt + g + (e >> 1) * 8;
@@ -162,10 +172,10 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
         __syncthreads();  // the previous chunk is done with X, Xs, B, C, dt, cum
         // ---- load the chunk: x (Q x P), B and C (Q x N) straight into shared
         // memory by asynchronous 16-byte copies (all in flight at once)
-        for (int i = tid; i < kQ * kP / 8; i += 128) {
-            const int t = i / (kP / 8), c8 = (i % (kP / 8)) * 8;
+        for (int i = tid; i < kQ * kPC / 8; i += 128) {
+            const int t = i / (kPC / 8), c8 = (i % (kPC / 8)) * 8;
             const Tin *src = static_cast<const Tin *>(p.x) + ((long long)b * L + l0 + t) * xs_t +
-                             (long long)h * kP + c8;
+                             (long long)h * kP + p0 + c8;
             cp_async16(&sm.X[t][c8], src, 16);
         }
         for (int i = tid; i < 2 * kQ * N / 8; i += 128) {
@@ -229,9 +239,9 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
                 G[j][e] = s <= t ? G[j][e] * ex2(ct - sm.cum[s]) * sm.dt[s] : 0.f;
             }
         // ---- Y = M X (intra-chunk)
-        float Y[kP / 8][4];
+        float Y[kPC / 8][4];
 #pragma unroll
-        for (int j = 0; j < kP / 8; ++j) Y[j][0] = Y[j][1] = Y[j][2] = Y[j][3] = 0.f;
+        for (int j = 0; j < kPC / 8; ++j) Y[j][0] = Y[j][1] = Y[j][2] = Y[j][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < kQ / 16; ++kk) {
             // the accumulators of s-tiles 2kk, 2kk+1 are the A fragment of k-step kk
@@ -241,36 +251,36 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
             af[2] = pack_bf16(G[2 * kk + 1][0], G[2 * kk + 1][1]);
             af[3] = pack_bf16(G[2 * kk + 1][2], G[2 * kk + 1][3]);
 #pragma unroll
-            for (int j = 0; j < kP / 8; j += 2) {
+            for (int j = 0; j < kPC / 8; j += 2) {
                 uint32_t bf[4];
-                load_b_kn(bf, &sm.X[0][0], kP + kPad, 8 * j, 16 * kk, lane);
+                load_b_kn(bf, &sm.X[0][0], kPC + kPad, 8 * j, 16 * kk, lane);
                 mma16816(Y[j], af, bf[0], bf[1]);
                 mma16816(Y[j + 1], af, bf[2], bf[3]);
             }
         }
         // ---- + exp(cum_t) C H_prev^T (state from before the chunk; hi and lo parts)
         {
-            float Z[kP / 8][4];
+            float Z[kPC / 8][4];
 #pragma unroll
-            for (int j = 0; j < kP / 8; ++j) Z[j][0] = Z[j][1] = Z[j][2] = Z[j][3] = 0.f;
+            for (int j = 0; j < kPC / 8; ++j) Z[j][0] = Z[j][1] = Z[j][2] = Z[j][3] = 0.f;
 #pragma unroll
             for (int k0 = 0; k0 < N; k0 += 16) {
                 uint32_t af[4];
                 load_a(af, &sm.Cm[0][0], N + kPad, t0, k0, lane);
 #pragma unroll
-                for (int j = 0; j < kP / 8; j += 2) {
+                for (int j = 0; j < kPC / 8; j += 2) {
                     uint32_t bf[4];
-                    load_b_kn(bf, &sm.Hh[0][0], kP + kPad, 8 * j, k0, lane);
+                    load_b_kn(bf, &sm.Hh[0][0], kPC + kPad, 8 * j, k0, lane);
                     mma16816(Z[j], af, bf[0], bf[1]);
                     mma16816(Z[j + 1], af, bf[2], bf[3]);
-                    load_b_kn(bf, &sm.Hl[0][0], kP + kPad, 8 * j, k0, lane);
+                    load_b_kn(bf, &sm.Hl[0][0], kPC + kPad, 8 * j, k0, lane);
                     mma16816(Z[j], af, bf[0], bf[1]);
                     mma16816(Z[j + 1], af, bf[2], bf[3]);
                 }
             }
             const float f0 = ex2(cum_r0), f1 = ex2(cum_r1);
 #pragma unroll
-            for (int j = 0; j < kP / 8; ++j) {
+            for (int j = 0; j < kPC / 8; ++j) {
                 Y[j][0] = fmaf(f0, Z[j][0], Y[j][0]);
                 Y[j][1] = fmaf(f0, Z[j][1], Y[j][1]);
                 Y[j][2] = fmaf(f1, Z[j][2], Y[j][2]);
@@ -279,7 +289,7 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
         }
         // ---- + D x, store y
 #pragma unroll
-        for (int j = 0; j < kP / 8; ++j)
+        for (int j = 0; j < kPC / 8; ++j)
 #pragma unroll
             for (int e = 0; e < 4; e += 2) {
                 const int t = t0 + g + (e >> 1) * 8, pp = 8 * j + 2 * tg;
@@ -287,14 +297,14 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
                 const float y0 = fmaf(Dh, bf16lo(xw), Y[j][e]);
                 const float y1 = fmaf(Dh, bf16hi(xw), Y[j][e + 1]);
                 Tout *dst = static_cast<Tout *>(p.y) + ((long long)b * L + l0 + t) * xs_t +
-                            (long long)h * kP + pp;
+                            (long long)h * kP + p0 + pp;
                 store_pair(dst, y0, y1);
             }
 
         // ---- carry: H = exp(cum_last) H + B^T (x scaled by exp(cum_last - cum_s) dt_s)
         const float cum_last = sm.cum[kQ - 1];
-        for (int i = tid; i < kQ * kP / 2; i += 128) {
-            const int s = i / (kP / 2), pp = (i % (kP / 2)) * 2;
+        for (int i = tid; i < kQ * kPC / 2; i += 128) {
+            const int s = i / (kPC / 2), pp = (i % (kPC / 2)) * 2;
             const float w = ex2(cum_last - sm.cum[s]) * sm.dt[s];
             const uint32_t xw = *reinterpret_cast<const uint32_t *>(&sm.X[s][pp]);
             *reinterpret_cast<uint32_t *>(&sm.Xs[s][pp]) = pack_bf16(bf16lo(xw) * w, bf16hi(xw) * w);
@@ -304,7 +314,7 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-            for (int pt = 0; pt < kP / 8; ++pt)
+            for (int pt = 0; pt < kPC / 8; ++pt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) Hacc[mt][pt][e] *= decay;
 #pragma unroll
@@ -312,9 +322,9 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
                 uint32_t af[4];
                 load_a_t(af, &sm.Bm[0][0], N + kPad, NW * warp + 16 * mt, k0, lane);
 #pragma unroll
-                for (int pt = 0; pt < kP / 8; pt += 2) {
+                for (int pt = 0; pt < kPC / 8; pt += 2) {
                     uint32_t bf[4];
-                    load_b_kn(bf, &sm.Xs[0][0], kP + kPad, 8 * pt, k0, lane);
+                    load_b_kn(bf, &sm.Xs[0][0], kPC + kPad, 8 * pt, k0, lane);
                     mma16816(Hacc[mt][pt], af, bf[0], bf[1]);
                     mma16816(Hacc[mt][pt + 1], af, bf[2], bf[3]);
                 }
@@ -327,11 +337,11 @@ __global__ void __launch_bounds__(128) ssd_fwd_kernel(const ssh::SsdParams p) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int pt = 0; pt < kP / 8; ++pt)
+            for (int pt = 0; pt < kPC / 8; ++pt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int n = NW * warp + 16 * mt + g + (e >> 1) * 8;
-                    const int pp = 8 * pt + 2 * tg + (e & 1);
+                    const int pp = p0 + 8 * pt + 2 * tg + (e & 1);
                     p.h_last[(((long long)b * p.heads + h) * kP + pp) * N + n] = Hacc[mt][pt][e];
                 }
     }
@@ -350,7 +360,7 @@ int ssd_n(const ssh::SsdParams &p, cudaStream_t st) {
             return SS_ERR_CUDA;
         done[dev] = true;
     }
-    kern<<<(unsigned)((long long)p.batch * p.heads), 128, smem, st>>>(p);
+    kern<<<(unsigned)((long long)p.batch * p.heads * (kP / kPC)), 128, smem, st>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
@@ -367,7 +377,7 @@ int ssd_t(const ssh::SsdParams &p, cudaStream_t st) {
 
 bool ssh::ssd_supported(const ssh::SsdParams &p) {
     return p.in_dtype == SS_BF16 && p.headdim == kP && (p.dstate == 64 || p.dstate == 128) && p.seqlen % kQ == 0 &&
-           (long long)p.batch * p.heads < (1LL << 31);
+           (long long)p.batch * p.heads * (kP / kPC) < (1LL << 31);
 }
 
 int ssh::launch_ssd(const ssh::SsdParams &p, cudaStream_t st) {
