@@ -200,7 +200,7 @@ def probe_alu(device):
     lib.ss_probe_alu.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(ctypes.c_double)]
     out = {}
-    for which, name in ((0, "ex2"), (1, "ffma"), (2, "ffma2"), (3, "mixed")):
+    for which, name in ((0, "ex2"), (1, "ffma"), (2, "ffma2"), (3, "mixed"), (4, "mma_sync_bf16")):
         r, g = ctypes.c_double(), ctypes.c_double()
         rc = lib.ss_probe_alu(which, device, ctypes.byref(r), ctypes.byref(g))
         out[name] = {"ops_per_s": r.value, "sm_ghz": g.value, "rc": rc}
@@ -403,7 +403,7 @@ def time_bwd(ss, ctx, dev, stream, cfg, d, params, args):
             "hbm_peak_source": src, "steps": steps, "gpu_launches": steps}
 
 
-def time_ssd(ss, ctx, dev, stream, args, batch=8, L=2048, H=80, P=64, N=128):
+def time_ssd(ss, ctx, dev, stream, args, batch=8, L=2048, H=80, P=64, N=128, probes=None):
     """Time ss_ssd_fwd on the Mamba-2 block shape (d_inner 5120 = 80 heads of
     64, d_state 128), bf16 inputs, fp32 y."""
     import ctypes
@@ -448,12 +448,20 @@ def time_ssd(ss, ctx, dev, stream, args, batch=8, L=2048, H=80, P=64, N=128):
     except Exception:
         peak_t = 1800.0
     hbm, src = measured_peaks()
+    legacy = None
+    m = (probes or {}).get("mma_sync_bf16")
+    if m and m.get("rc") == 0 and m.get("sm_ghz", 0) > 0:
+        # what mma.sync (the tensor-core path this kernel uses) sustains, at the maximum clock
+        lp = m["ops_per_s"] * (MAX_SM_MHZ * 1e-3) / m["sm_ghz"] / 1e12
+        legacy = {"peak_tflops": lp, "frac": tflops / lp,
+                  "note": "mma.sync m16n8k16 bf16 probe, independent accumulators, 64 warps/SM"}
     return {"workload": "ssd (Mamba-2): batch %d, L %d, %d heads x %d, d_state %d, bf16 in, "
                         "fp32 y, chunk %d" % (batch, L, H, P, N, Q),
             "us_per_call": us, "elements_per_s": batch * L * H * P / (us * 1e-6),
             "tensor": {"achieved_tflops": tflops, "peak_tflops": peak_t,
                        "frac": tflops / peak_t, "note": "algorithmic bf16 products (the state's "
-                       "low bf16 half in C H_prev adds 2 Q P N per chunk, not counted)"},
+                       "low bf16 half in C H_prev adds 2 Q P N per chunk, not counted)",
+                       "legacy_mma": legacy},
             "hbm": {"gbs": nbytes / (us * 1e-6) / 1e9, "peak": hbm, "peak_source": src,
                     "frac": nbytes / (us * 1e-6) / 1e9 / hbm},
             "steps": steps, "gpu_launches": steps}
@@ -552,7 +560,7 @@ def run_ours(args, rank, world, local):
     decode = None if args.skip_decode else time_decode(ss, ctx, dev, stream, args)
     conv1d = None if args.skip_conv else time_conv1d(ss, ctx, dev, stream, cfg, args)
     bwd = None if args.skip_bwd else time_bwd(ss, ctx, dev, stream, cfg, d, params, args)
-    ssd = None if args.skip_ssd else time_ssd(ss, ctx, dev, stream, args)
+    ssd = None if args.skip_ssd else time_ssd(ss, ctx, dev, stream, args, probes=probes)
 
     # ---- end to end: pinned host inputs in, y and h_last back to host, every step.
     # Steps are pipelined over two buffer sets and three streams: the inputs of

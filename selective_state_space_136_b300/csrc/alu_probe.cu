@@ -34,10 +34,20 @@ __device__ __forceinline__ void ffma2(float &a0, float &a1, float b0, float b1, 
         : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 template <int WHICH>
 __global__ void __launch_bounds__(256) probe_kernel(float *sink, int iters,
                                                     unsigned long long *clk) {
-    float a[8], c[16];
+    float a[8], c[16], acc[8][4] = {};
+    const uint32_t fa = 0x3f803f80u + threadIdx.x, fb = 0x3f003f00u;  // bf16 pairs near 1 and 0.5
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = 0.25f + 0.01f * i + 1e-6f * threadIdx.x;
 #pragma unroll
@@ -53,6 +63,9 @@ __global__ void __launch_bounds__(256) probe_kernel(float *sink, int iters,
             } else if constexpr (WHICH == 1) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) a[i] = fmaf(a[i], 0.9990234375f, 0.0009765625f);
+            } else if constexpr (WHICH == 4) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mma_bf16(acc[i], fa, fa, fa, fa, fb, fb);
             } else if constexpr (WHICH == 2) {
 #pragma unroll
                 for (int i = 0; i < 8; i += 2)
@@ -79,6 +92,8 @@ __global__ void __launch_bounds__(256) probe_kernel(float *sink, int iters,
     for (int i = 0; i < 8; ++i) s += a[i];
 #pragma unroll
     for (int i = 0; i < 16; ++i) s += c[i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += acc[i][0] + acc[i][1] + acc[i][2] + acc[i][3];
     if (s == 1234.5f) sink[threadIdx.x] = s;  // keeps the chains live
 }
 
@@ -87,7 +102,8 @@ __global__ void __launch_bounds__(256) probe_kernel(float *sink, int iters,
 extern "C" {
 
 // which: 0 = MUFU ex2, 1 = FFMA, 2 = packed FFMA2 (counted as 2 FMA each),
-// 3 = mixed (counted in ex2: each ex2 comes with four FMA lane-ops).
+// 3 = mixed (counted in ex2: each ex2 comes with four FMA lane-ops),
+// 4 = legacy tensor-core mma.sync m16n8k16 bf16 with fp32 accumulation (flops).
 // Writes the sustained rate in operations per second and the SM clock in GHz
 // seen by the probe. Returns 0 on success, the CUDA error code otherwise.
 int ss_probe_alu_occ(int which, int device, int warps_per_sm, double *ops_per_s,
@@ -101,7 +117,7 @@ int ss_probe_alu(int which, int device, double *ops_per_s, double *sm_ghz) {
 // 256 threads, one wave): what a scheduler sustains with few warps to pick from.
 int ss_probe_alu_occ(int which, int device, int warps_per_sm, double *ops_per_s,
                      double *sm_ghz) {
-    if (warps_per_sm < 1 || warps_per_sm > 64 || which < 0 || which > 3) return -1;
+    if (warps_per_sm < 1 || warps_per_sm > 64 || which < 0 || which > 4) return -1;
     cudaError_t e = cudaSetDevice(device);
     if (e != cudaSuccess) return (int)e;
     int sms = 0;
@@ -122,7 +138,8 @@ int ss_probe_alu_occ(int which, int device, int warps_per_sm, double *ops_per_s,
         if (which == 0) probe_kernel<0><<<blocks, threads, 0, st>>>(sink, n, clk);
         else if (which == 1) probe_kernel<1><<<blocks, threads, 0, st>>>(sink, n, clk);
         else if (which == 2) probe_kernel<2><<<blocks, threads, 0, st>>>(sink, n, clk);
-        else probe_kernel<3><<<blocks, threads, 0, st>>>(sink, n, clk);
+        else if (which == 3) probe_kernel<3><<<blocks, threads, 0, st>>>(sink, n, clk);
+        else probe_kernel<4><<<blocks, threads, 0, st>>>(sink, n, clk);
     };
     run(iters / 8);  // warm-up
     cudaEventRecord(a, st);
@@ -134,7 +151,10 @@ int ss_probe_alu_occ(int which, int device, int warps_per_sm, double *ops_per_s,
     if (e == cudaSuccess) {
         cudaEventElapsedTime(&ms, a, b);
         cudaMemcpy(hc, clk, sizeof(hc), cudaMemcpyDeviceToHost);
-        const double ops = (double)blocks * threads * iters * 32.0;  // 4 x 8 per iteration
+        // 4 x 8 operations per thread and iteration; for the mma probe 4 x 8
+        // m16n8k16 products of 4096 flops per warp and iteration
+        const double ops = which == 4 ? (double)blocks * (threads / 32) * iters * 32.0 * 4096.0
+                                      : (double)blocks * threads * iters * 32.0;
         if (ops_per_s) *ops_per_s = ops / (ms * 1e-3);
         if (sm_ghz) *sm_ghz = hc[1] ? (double)hc[0] / (double)hc[1] : 0.0;
     }
