@@ -25,7 +25,7 @@ def _close(got, ref, bf16, what):
 
 @pytest.mark.parametrize("N,L,dim,dt", [(16, 64, 48, "f32"), (16, 32, 70, "bf16"),
                                         (4, 48, 33, "f32"), (1, 16, 32, "f32"),
-                                        (8, 128, 96, "bf16")])
+                                        (8, 128, 96, "bf16"), (2, 32, 40, "bf16")])
 @pytest.mark.parametrize("full", [True, False])
 def test_bwd_matches_oracle(N, L, dim, dt, full):
     """Every gradient, with (full) and without the optional inputs."""
@@ -53,6 +53,31 @@ def test_bwd_matches_oracle(N, L, dim, dt, full):
         _close(got[k], ref[k], bf, k)
     if not full:
         assert got["dz"] is None and got["dD"] is None and got["dh0"] is None
+
+
+@pytest.mark.parametrize("N", [16, 1])
+def test_bwd_without_softplus(N):
+    """dt = delta + bias taken as is: ddelta is then the dt gradient itself."""
+    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=2, dim=40, dstate=N, seqlen=48,
+                           in_dtype="f32", seed=140 + N)
+    inp = workloads.scan_inputs(cfg, with_h0=True)
+    # keep dt = delta + bias positive and moderate when used as is
+    inp["delta"] = (np.abs(inp["delta"]) * 0.05).astype(np.float32)
+    inp["delta_bias"] = np.full_like(inp["delta_bias"], 0.01)
+    t = device_inputs(inp, cfg)
+    g = np.random.default_rng(8)
+    dy = g.standard_normal((cfg.batch, cfg.dim, cfg.seqlen))
+    got = ss.ss_scan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"],
+                         torch.from_numpy(dy.astype(np.float32)).cuda(), D=t["D"],
+                         delta_bias=t["delta_bias"], z=t["z"], delta_softplus=False)
+    torch.cuda.synchronize()
+    shp = (cfg.batch, cfg.dim, cfg.seqlen)
+    ref = oracle.scan_bwd(inp["u"].reshape(shp), inp["delta"].reshape(shp), inp["A"], inp["B"],
+                          inp["C"], dy.astype(np.float32).astype(np.float64), D=inp["D"],
+                          delta_bias=inp["delta_bias"], z=inp["z"].reshape(shp),
+                          delta_softplus=False)
+    for k in ("du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias"):
+        _close(got[k], ref[k], False, k)
 
 
 def test_bwd_long_rows():
