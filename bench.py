@@ -424,17 +424,27 @@ def time_ssd(ss, ctx, dev, stream, args, batch=8, L=2048, H=80, P=64, N=128, pro
                    y.data_ptr(), hl.data_ptr())
     fn, argp = ss.lib().ss_ssd_fwd, ctypes.byref(a)
     sp = ctypes.c_void_p(stream.cuda_stream)
-    for _ in range(max(args.warmup, 3)):
-        assert fn(ctx.handle, argp, sp) == 0
-    torch.cuda.synchronize(dev)
     steps = max(args.steps, 1)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        fn(ctx.handle, argp, sp)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    us = e0.elapsed_time(e1) * 1e3 / steps
+
+    def timed(handle):
+        for _ in range(max(args.warmup, 3)):
+            assert fn(handle, argp, sp) == 0
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn(handle, argp, sp)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / steps
+
+    # the tensor-memory (tcgen05) kernel on the same call, for comparison
+    tc_ctx = ss.Context(dev.index if dev.index is not None else 0)
+    tc_ctx.set_option(ss.SS_OPT_SSD_PATH, ss.SS_SSD_PATH_TCGEN05)
+    us_tc = timed(tc_ctx.handle)
+    tc_ctx.close()
+    us = timed(ctx.handle)
+    path = "tensor memory (tcgen05)" if ctx.last_launch()[0] == 1 else "mma.sync"
     Q = 64
     chunks = batch * H * (L // Q)
     # per chunk and head: C B^T (2 Q Q N), masked products with x (2 Q Q P),
@@ -456,8 +466,10 @@ def time_ssd(ss, ctx, dev, stream, args, batch=8, L=2048, H=80, P=64, N=128, pro
         legacy = {"peak_tflops": lp, "frac": tflops / lp,
                   "note": "mma.sync m16n8k16 bf16 probe, independent accumulators, 64 warps/SM"}
     return {"workload": "ssd (Mamba-2): batch %d, L %d, %d heads x %d, d_state %d, bf16 in, "
-                        "fp32 y, chunk %d" % (batch, L, H, P, N, Q),
-            "us_per_call": us, "elements_per_s": batch * L * H * P / (us * 1e-6),
+                        "fp32 y" % (batch, L, H, P, N),
+            "flops_counted_at_chunk": Q,
+            "kernel": path, "us_per_call": us, "tcgen05_kernel_us_per_call": us_tc,
+            "elements_per_s": batch * L * H * P / (us * 1e-6),
             "tensor": {"achieved_tflops": tflops, "peak_tflops": peak_t,
                        "frac": tflops / peak_t, "note": "algorithmic bf16 products (the state's "
                        "low bf16 half in C H_prev adds 2 Q P N per chunk, not counted)",

@@ -343,6 +343,15 @@ const char *ss_status_string(int status);
  *   SS_OPT_TEST_DROP_TILE   test hook: the rows kernel never issues the loads
  *                           of this tile index, so its wait runs out and the
  *                           timeout path is exercised (-1 = off, the default).
+ *   SS_OPT_SSD_PATH         tensor-core kernel of ss_ssd_fwd:
+ *                           SS_SSD_PATH_AUTO (default) and SS_SSD_PATH_MMA_SYNC
+ *                           run the warp-level mma.sync kernel (64-step
+ *                           chunks), the faster of the two at the Mamba-2
+ *                           block shape; SS_SSD_PATH_TCGEN05 runs the
+ *                           tensor-memory kernel (tcgen05 products with
+ *                           accumulators in tensor memory, 128-step chunks;
+ *                           headdim 64, dstate 128, seqlen a multiple of 128,
+ *                           else SS_ERR_UNSUPPORTED).
  * Returns SS_OK or SS_ERR_INVALID_ARG (unknown option or value out of range).
  */
 typedef enum {
@@ -359,8 +368,15 @@ typedef enum {
     SS_OPT_WAIT_LIMIT = 3,
     SS_OPT_TEST_DROP_TILE = 4,
     SS_OPT_RESIDENT_WARPS = 5,
-    SS_OPT_DISCRETIZATION = 6
+    SS_OPT_DISCRETIZATION = 6,
+    SS_OPT_SSD_PATH = 7
 } ss_option;
+
+typedef enum {
+    SS_SSD_PATH_AUTO = 0,
+    SS_SSD_PATH_MMA_SYNC = 1,
+    SS_SSD_PATH_TCGEN05 = 2
+} ss_ssd_path;
 
 typedef enum { SS_DISC_SIMPLIFIED = 0, SS_DISC_ZOH = 1 } ss_discretization;
 
@@ -369,7 +385,8 @@ int ss_set_option(ss_ctx *ctx, int option, long long value);
 /*
  * Describe the last ss_scan_fwd / ss_state_update enqueued on this context:
  * *variant receives the ss_variant that ran, *launches the number of kernels
- * it enqueued. Either pointer may be NULL.
+ * it enqueued. After ss_ssd_fwd, *variant is 1 for the tensor-memory kernel
+ * and 0 for the mma.sync kernel. Either pointer may be NULL.
  */
 int ss_last_launch(const ss_ctx *ctx, int *variant, int *launches);
 

@@ -22,8 +22,9 @@ SS_F32, SS_BF16 = 0, 1
 SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_CUDA, SS_ERR_TIMEOUT, SS_ERR_DEVICE = range(6)
 SS_VARIANT_AUTO, SS_VARIANT_ROWS, SS_VARIANT_CHUNKED, SS_VARIANT_SIMPLE = range(4)
 (SS_OPT_VARIANT, SS_OPT_SEGMENTS, SS_OPT_THREADS_PER_ROW, SS_OPT_WAIT_LIMIT,
- SS_OPT_TEST_DROP_TILE, SS_OPT_RESIDENT_WARPS, SS_OPT_DISCRETIZATION) = range(7)
+ SS_OPT_TEST_DROP_TILE, SS_OPT_RESIDENT_WARPS, SS_OPT_DISCRETIZATION, SS_OPT_SSD_PATH) = range(8)
 SS_DISC_SIMPLIFIED, SS_DISC_ZOH = range(2)
+SS_SSD_PATH_AUTO, SS_SSD_PATH_MMA_SYNC, SS_SSD_PATH_TCGEN05 = range(3)
 
 _vp = ctypes.c_void_p
 

@@ -27,7 +27,7 @@ FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcomp
 LIBS = {
     # library name -> sources
     "libss_scan.so": ["ss_api.cu", "ss_simple.cu", "ss_update.cu", "ss_rows.cu",
-                      "ss_seq.cu", "ss_pair.cu", "ss_noalloc.cu", "ss_conv.cu", "ss_bwd.cu", "ss_ssd.cu"],
+                      "ss_seq.cu", "ss_pair.cu", "ss_noalloc.cu", "ss_conv.cu", "ss_bwd.cu", "ss_ssd.cu", "ss_ssd_tc.cu"],
     "libss_probe.so": ["alu_probe.cu"],
 }
 

@@ -149,6 +149,10 @@ int ss_set_option(ss_ctx *ctx, int option, long long value) {
             if (value < -1 || value > (1LL << 30)) return SS_ERR_INVALID_ARG;
             ctx->drop_tile = (int)value;
             return SS_OK;
+        case SS_OPT_SSD_PATH:
+            if (value < SS_SSD_PATH_AUTO || value > SS_SSD_PATH_TCGEN05) return SS_ERR_INVALID_ARG;
+            ctx->ssd_path = (int)value;
+            return SS_OK;
         default: return SS_ERR_INVALID_ARG;
     }
 }
@@ -433,11 +437,13 @@ int ss_ssd_fwd(ss_ctx *ctx, const ss_ssd_args *a, ss_stream_t stream) {
         return SS_ERR_INVALID_ARG;
     ssh::SsdParams p{a->batch, a->heads, a->headdim, a->dstate, a->seqlen, a->in_dtype,
                      a->out_dtype, a->x, a->dt, a->A, a->B, a->C, a->D, a->dt_bias,
-                     a->dt_softplus, a->h0, a->y, a->h_last};
-    if (!ssh::ssd_supported(p)) return SS_ERR_UNSUPPORTED;
+                     a->dt_softplus, a->h0, a->y, a->h_last, ctx->d_err, ctx->wait_limit};
+    const bool tc = ctx->ssd_path == SS_SSD_PATH_TCGEN05;
+    if (tc ? !ssh::ssd_tc_supported(p) : !ssh::ssd_supported(p)) return SS_ERR_UNSUPPORTED;
     if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
-    const int rc = ssh::launch_ssd(p, reinterpret_cast<cudaStream_t>(stream));
-    ctx->last_variant = 0;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int rc = tc ? ssh::launch_ssd_tc(p, st) : ssh::launch_ssd(p, st);
+    ctx->last_variant = tc ? 1 : 0;
     ctx->last_launches = rc == SS_OK ? 1 : 0;
     return rc;
 }

@@ -23,6 +23,7 @@ struct ss_ctx {
     uint32_t wait_limit = 1u << 22;  // polls before a device wait gives up
     int drop_tile = -1;            // test hook: a tile whose loads are never issued
     int zoh = 0;                   // SS_DISC_ZOH: exact zero-order-hold input matrix
+    int ssd_path = SS_SSD_PATH_AUTO;
     void *bwd_scratch = nullptr;   // backward checkpoints, grown on demand
     size_t bwd_scratch_bytes = 0;
     int last_variant = 0;
@@ -127,9 +128,13 @@ struct SsdParams {
     const float *h0;
     void *y;
     float *h_last;
+    int *err;             // device error word (SS_ERR_TIMEOUT when a wait gives up)
+    uint32_t wait_limit;  // polls before a device-side wait gives up
 };
 bool ssd_supported(const SsdParams &p);
 int launch_ssd(const SsdParams &p, cudaStream_t st);
+bool ssd_tc_supported(const SsdParams &p);
+int launch_ssd_tc(const SsdParams &p, cudaStream_t st);
 
 // causal depthwise conv1d (ss_conv.cu)
 struct ConvParams {

@@ -1,0 +1,511 @@
+// Mamba-2 state space duality (SSD) forward on the fifth-generation tensor
+// cores: tcgen05 products with operands in shared memory and accumulators in
+// tensor memory (TMEM).
+//
+// The computation is the chunked block decomposition of soft186.com,
+// "Mamba选择性状态空间机制", section "状态空间对偶性算法突破" (the selective
+// recurrence with A = a_h I per head, dt shared by the head's P channels, B and
+// C shared by all heads), the same as the mma.sync kernel in ss_ssd.cu, with
+// Q = 128-step chunks so that every product has M = 128 rows (one TMEM lane
+// per row). Per chunk, with cum_t the running sum of dt_r a (log2 units):
+//   G  = C B^T                                  (t x s over n)      -> TMEM
+//   M  = G o exp2(cum_t - cum_s) dt_s, s <= t   (bf16, shared memory)
+//   Y  = M X                                    (t x p over s)      -> TMEM
+//   Z  = C H_prev                               (t x p over n; H as bf16 hi + lo)
+//   y  = Y + exp2(cum_t) Z + D x
+//   S  = exp2(cum_last) S + B^T Xs,  Xs[s] = x_s exp2(cum_last - cum_s) dt_s
+// where S[n][p] is the carried state, kept in fp32 in TMEM for the whole row
+// of chunks and copied to shared memory as bf16 hi + lo for the next Z.
+//
+// One CTA of 8 warps per (batch, head). Warp w reads TMEM lanes
+// [32 (w % 4), 32 (w % 4) + 32) (rows t of G, Y, Z; rows n of S) and takes half
+// w / 4 of each epilogue's columns. Thread 0 issues the MMAs and commits them
+// to one mbarrier; the other threads meanwhile build Xs and rescale S. C and B
+// are double-buffered and the next chunk's x and dt wait in registers, so a
+// chunk's loads overlap the previous chunk's work. Shared
+// operand tiles are stored as 8-row x 16-byte core matrices, column blocks
+// fastest, and described to the tensor core without swizzling: K-major tiles
+// (C, B, M) with the leading offset between K-adjacent core matrices and the
+// stride offset between 8-row groups; MN-major tiles (X, Xs, H, and B read as
+// B^T) the other way round.
+#include "ss_common.cuh"
+#include "ss_internal.h"
+
+namespace {
+
+using namespace ssk;
+
+constexpr int kQ = 128;  // chunk length = MMA rows
+constexpr int kP = 64;   // head dimension
+constexpr int kN = 128;  // state size
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColG = 0;    // G (128 columns); then Z (64)
+constexpr uint32_t kColY = 128;  // Y (64)
+constexpr uint32_t kColS = 192;  // carried state S (64)
+
+struct TcSmem {
+    uint16_t C[2][kQ * kN];  // C of the chunk [t][n], K-major for G and Z (two buffers)
+    uint16_t B[2][kQ * kN];  // B of the chunk [s][n]: K-major for G, MN-major (B^T) for S
+    uint16_t M[kQ * kQ];     // masked G [t][s], K-major for Y
+    uint16_t X[kQ * kP];     // x of the chunk [s][p], MN-major for Y
+    uint16_t Xs[kQ * kP];    // scaled x [s][p], MN-major for S
+    uint16_t Hh[kN * kP];    // carried state, high bf16 part [n][p], MN-major for Z
+    uint16_t Hl[kN * kP];    // carried state, low part (S - hi)
+    float dt[kQ];
+    float cum[kQ];
+    uint64_t bar;
+    uint32_t tmem;
+};
+
+// Byte offset of element (r, c) of a bf16 tile with `cols` columns stored as
+// 8-row x 16-byte core matrices, the column blocks of an 8-row group adjacent.
+__device__ __forceinline__ uint32_t cm_off(int r, int c, int cols) {
+    return ((((r >> 3) * (cols >> 3)) + (c >> 3)) << 7) + ((r & 7) << 4) + ((c & 7) << 1);
+}
+
+// Shared-memory matrix descriptor without swizzling: start address, leading
+// and stride byte offsets (all in 16-byte units), descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc(const void *p, uint32_t byte_off, uint32_t lbo,
+                                          uint32_t sbo) {
+    const uint32_t a = smem_u32(p) + byte_off;
+    return (uint64_t)((a >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A/B
+// MN-major flags, N >> 3 and M >> 4.
+constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+constexpr uint32_t kIdG = idesc_bf16(kQ, kQ, 0, 0);  // G: C (K-major) x B (K-major)
+constexpr uint32_t kIdY = idesc_bf16(kQ, kP, 0, 1);  // Y, Z: K-major A x MN-major B
+constexpr uint32_t kIdS = idesc_bf16(kN, kP, 1, 1);  // S: B^T (MN-major) x Xs (MN-major)
+// descriptor offsets (bytes)
+constexpr uint32_t kKmLbo = 128, kKmSbo = 128 * (kQ / 8);  // K-major 128-column tiles
+constexpr uint32_t kKmStep = 256;                          // 16 columns of K
+constexpr uint32_t kMn64Lbo = 128 * (kP / 8), kMn64Sbo = 128, kMn64Step = 2 * kMn64Lbo;
+constexpr uint32_t kMn128Lbo = 128 * (kN / 8), kMn128Sbo = 128, kMn128Step = 2 * kMn128Lbo;
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t id,
+                                        bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(ad), "l"(bd), "r"(id), "r"((uint32_t)accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane; the wait is part of
+// the same statement, so the registers are valid when it returns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];\n\ttcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    return a | (b << 16);
+}
+__device__ __forceinline__ float round_bf16(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// Row n of the state (16 columns at p0) as bf16 hi and lo parts into Hh / Hl.
+__device__ __forceinline__ void put_state16(uint8_t *hh, uint8_t *hl, int n, int p0,
+                                            const float (&v)[16]) {
+    uint32_t wh[8], wl[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float h0 = round_bf16(v[2 * j]), h1 = round_bf16(v[2 * j + 1]);
+        wh[j] = pack2(h0, h1);
+        wl[j] = pack2(v[2 * j] - h0, v[2 * j + 1] - h1);
+    }
+    *reinterpret_cast<uint4 *>(hh + cm_off(n, p0, kP)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+    *reinterpret_cast<uint4 *>(hh + cm_off(n, p0 + 8, kP)) = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+    *reinterpret_cast<uint4 *>(hl + cm_off(n, p0, kP)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    *reinterpret_cast<uint4 *>(hl + cm_off(n, p0 + 8, kP)) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+}
+
+__device__ __forceinline__ void store16(float *dst, const float (&v)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        reinterpret_cast<float4 *>(dst)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+__device__ __forceinline__ void store16(uint16_t *dst, const float (&v)[16]) {
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = pack2(v[2 * j], v[2 * j + 1]);
+    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+constexpr int kThreads = 256;  // 8 warps: warp w serves TMEM lanes 32 (w % 4) .. +32 and
+                               // column half w / 4 of each epilogue
+
+template <typename Tout>
+__global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    TcSmem &sm = *reinterpret_cast<TcSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint8_t *sM = reinterpret_cast<uint8_t *>(sm.M), *sX = reinterpret_cast<uint8_t *>(sm.X);
+    uint8_t *sXs = reinterpret_cast<uint8_t *>(sm.Xs);
+    uint8_t *sHh = reinterpret_cast<uint8_t *>(sm.Hh), *sHl = reinterpret_cast<uint8_t *>(sm.Hl);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = 32 * quarter + lane;  // this thread's TMEM lane: row t of G, Y, Z; row n of S
+    const int b = blockIdx.x / p.heads, h = blockIdx.x % p.heads;
+    const long long L = p.seqlen;
+    const float a = p.A[h] * kLog2e;  // log2 units
+    const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
+    const float Dh = p.D ? p.D[h] : 0.f;
+    const long long xs_t = (long long)p.heads * kP;  // x / y stride between steps
+    const uint16_t *gx = static_cast<const uint16_t *>(p.x);
+    const uint16_t *gB = static_cast<const uint16_t *>(p.B);
+    const uint16_t *gC = static_cast<const uint16_t *>(p.C);
+    const uint16_t *gdt = static_cast<const uint16_t *>(p.dt);
+    const long long st_base = ((long long)b * p.heads + h) * kP * kN;  // h0 / h_last (p, n)
+    const int n_chunks = (int)(L / kQ);
+
+    // C and B of chunk c into buffer c & 1 (16-byte asynchronous copies, one group)
+    auto issue_cb = [&](int c) {
+        uint8_t *dC = reinterpret_cast<uint8_t *>(sm.C[c & 1]);
+        uint8_t *dB = reinterpret_cast<uint8_t *>(sm.B[c & 1]);
+        const long long l0 = (long long)c * kQ;
+#pragma unroll
+        for (int k = 0; k < kQ * kN / 8 / kThreads; ++k) {
+            const int i = tid + kThreads * k, t = i % kQ, n8 = i / kQ;
+            const long long g = ((long long)b * L + l0 + t) * kN + 8 * n8;
+            cp_async16(dC + cm_off(t, 8 * n8, kN), gC + g, 16);
+            cp_async16(dB + cm_off(t, 8 * n8, kN), gB + g, 16);
+        }
+        cp_async_commit();
+    };
+    // x of chunk c: this thread's four 16-byte pieces, into registers
+    constexpr int kXPieces = kQ * kP / 8 / kThreads;
+    auto load_x = [&](int c, uint4 (&xr)[kXPieces]) {
+        const long long l0 = (long long)c * kQ;
+#pragma unroll
+        for (int k = 0; k < kXPieces; ++k) {
+            const int i = tid + kThreads * k, s = i % kQ, p8 = i / kQ;
+            xr[k] = __ldg(reinterpret_cast<const uint4 *>(
+                gx + ((long long)b * L + l0 + s) * xs_t + (long long)h * kP + 8 * p8));
+        }
+    };
+    // raw dt of chunk c, four steps per lane of warp 0
+    auto load_dt = [&](int c, float (&dr)[4]) {
+        const long long l0 = (long long)c * kQ;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            dr[k] = to_f32(gdt[((long long)b * L + l0 + 4 * lane + k) * p.heads + h]);
+    };
+
+    if (warp == 0) {
+        asm volatile(
+            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                smem_u32(&sm.tmem)),
+            "r"(kTmemCols)
+            : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        mbar_init(&sm.bar, 1);
+        fence_mbar_init();
+    }
+    // The masked tile's 16-byte pieces right of a 32-row band are zero in every
+    // chunk (s > t there): written once.
+    for (int i = tid; i < kQ * kQ / 8; i += kThreads) {
+        const int t = i % kQ, s8 = i / kQ;
+        if (8 * s8 >= 32 * (t / 32 + 1))
+            *reinterpret_cast<uint4 *>(sM + cm_off(t, 8 * s8, kQ)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint4 xr[kXPieces];
+    float dr[4] = {0.f, 0.f, 0.f, 0.f};
+    if (n_chunks > 0) {
+        issue_cb(0);
+        load_x(0, xr);
+        if (warp == 0) load_dt(0, dr);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+    const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);  // this warp's lanes
+    const int c0 = 32 * half;  // this thread's columns of Y, Z and S
+
+    // initial state: row n = r, columns [c0, c0 + 32) of S (tensor memory) and Hh / Hl
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            v[i] = p.h0 ? p.h0[st_base + (long long)(c0 + 16 * j + i) * kN + r] : 0.f;
+        tmem_st16(trow + kColS + c0 + 16 * j, v);
+        put_state16(sHh, sHl, r, c0 + 16 * j, v);
+    }
+    tmem_wait_st();
+
+    uint32_t phase = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+        const long long l0 = (long long)c * kQ;
+        const uint8_t *sC = reinterpret_cast<const uint8_t *>(sm.C[c & 1]);
+        const uint8_t *sB = reinterpret_cast<const uint8_t *>(sm.B[c & 1]);
+        __syncthreads();  // every reader of the previous chunk's tiles is done
+        // ---- x of the chunk from registers into its tile; dt and its prefix sum
+#pragma unroll
+        for (int k = 0; k < kXPieces; ++k) {
+            const int i = tid + kThreads * k, s = i % kQ, p8 = i / kQ;
+            *reinterpret_cast<uint4 *>(sX + cm_off(s, 8 * p8, kP)) = xr[k];
+        }
+        if (warp == 0) {
+            float d4[4], c4[4], run = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float xv = dr[k] + bias;
+                d4[k] = p.softplus ? softplus1(xv) : xv;
+                run += d4[k] * a;
+                c4[k] = run;
+            }
+            float incl = run;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            const float before = incl - run;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                sm.dt[4 * lane + k] = d4[k];
+                sm.cum[4 * lane + k] = before + c4[k];
+            }
+        }
+        // ---- the next chunk's operands start moving now
+        if (c + 1 < n_chunks) {
+            issue_cb(c + 1);
+            load_x(c + 1, xr);
+            if (warp == 0) load_dt(c + 1, dr);
+            cp_async_wait<1>();  // this chunk's C and B have landed
+        } else {
+            cp_async_wait<0>();
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- G = C B^T into TMEM columns [0, 128)
+        if (tid == 0) {
+#pragma unroll
+            for (int k = 0; k < kN / 16; ++k)
+                mma_f16(tmem + kColG, sdesc(sC, k * kKmStep, kKmLbo, kKmSbo),
+                        sdesc(sB, k * kKmStep, kKmLbo, kKmSbo), kIdG, k > 0);
+            mma_commit(&sm.bar);
+        }
+        const float cum_last = sm.cum[kQ - 1];
+        // ---- meanwhile: Xs (row s = r, this half's 4 pieces) and S scaled by
+        // the chunk's decay in place (row r, this half's 32 columns)
+        {
+            const int s = r;
+            const float w = ex2(cum_last - sm.cum[s]) * sm.dt[s];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int p8 = 4 * half + k;
+                const uint4 v = *reinterpret_cast<const uint4 *>(sX + cm_off(s, 8 * p8, kP));
+                const uint4 o = make_uint4(pack2(bf16lo(v.x) * w, bf16hi(v.x) * w),
+                                           pack2(bf16lo(v.y) * w, bf16hi(v.y) * w),
+                                           pack2(bf16lo(v.z) * w, bf16hi(v.z) * w),
+                                           pack2(bf16lo(v.w) * w, bf16hi(v.w) * w));
+                *reinterpret_cast<uint4 *>(sXs + cm_off(s, 8 * p8, kP)) = o;
+            }
+            const float dec = ex2(cum_last);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float v[16];
+                tmem_ld16(trow + kColS + c0 + 16 * j, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] *= dec;
+                tmem_st16(trow + kColS + c0 + 16 * j, v);
+            }
+            tmem_wait_st();
+        }
+        if (__syncthreads_or(!mbar_wait_bounded(&sm.bar, phase, p.wait_limit))) {
+            if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
+            break;
+        }
+        phase ^= 1u;
+        tc_fence_after();
+
+        // ---- M = G o exp2(cum_t - cum_s) dt_s (s <= t), row t = r; the 16-column
+        // pieces left of and on this quarter's band, alternately to the two halves
+        {
+            const int t = r;
+            const float ct = sm.cum[t];
+            for (int j = half; j < 2 * (quarter + 1); j += 2) {
+                const int s0 = 16 * j;
+                float g[16];
+                tmem_ld16(trow + kColG + s0, g);
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int s = s0 + 2 * i;
+                    const float m0 = s <= t ? g[2 * i] * ex2(ct - sm.cum[s]) * sm.dt[s] : 0.f;
+                    const float m1 =
+                        s + 1 <= t ? g[2 * i + 1] * ex2(ct - sm.cum[s + 1]) * sm.dt[s + 1] : 0.f;
+                    w[i] = pack2(m0, m1);
+                }
+                *reinterpret_cast<uint4 *>(sM + cm_off(t, s0, kQ)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(sM + cm_off(t, s0 + 8, kQ)) =
+                    make_uint4(w[4], w[5], w[6], w[7]);
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- Y = M X, Z = C (Hh + Hl) (into G's columns), S += B^T Xs
+        if (tid == 0) {
+#pragma unroll
+            for (int k = 0; k < kQ / 16; ++k)
+                mma_f16(tmem + kColY, sdesc(sM, k * kKmStep, kKmLbo, kKmSbo),
+                        sdesc(sX, k * kMn64Step, kMn64Lbo, kMn64Sbo), kIdY, k > 0);
+#pragma unroll
+            for (int k = 0; k < kN / 16; ++k)
+                mma_f16(tmem + kColG, sdesc(sC, k * kKmStep, kKmLbo, kKmSbo),
+                        sdesc(sHh, k * kMn64Step, kMn64Lbo, kMn64Sbo), kIdY, k > 0);
+#pragma unroll
+            for (int k = 0; k < kN / 16; ++k)
+                mma_f16(tmem + kColG, sdesc(sC, k * kKmStep, kKmLbo, kKmSbo),
+                        sdesc(sHl, k * kMn64Step, kMn64Lbo, kMn64Sbo), kIdY, true);
+#pragma unroll
+            for (int k = 0; k < kQ / 16; ++k)
+                mma_f16(tmem + kColS, sdesc(sB, k * kMn128Step, kMn128Lbo, kMn128Sbo),
+                        sdesc(sXs, k * kMn64Step, kMn64Lbo, kMn64Sbo), kIdS, true);
+            mma_commit(&sm.bar);
+        }
+        if (__syncthreads_or(!mbar_wait_bounded(&sm.bar, phase, p.wait_limit))) {
+            if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
+            break;
+        }
+        phase ^= 1u;
+        tc_fence_after();
+
+        // ---- y row t = r, this half's 32 channels; the new state's row n = r
+        // (same columns) into Hh / Hl
+        {
+            const int t = r;
+            const float ft = ex2(sm.cum[t]);
+            Tout *dst = static_cast<Tout *>(p.y) + ((long long)b * L + l0 + t) * xs_t +
+                        (long long)h * kP + c0;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float yv[16], zv[16];
+                tmem_ld16(trow + kColY + c0 + 16 * j, yv);
+                tmem_ld16(trow + kColG + c0 + 16 * j, zv);
+                const uint4 x0 = *reinterpret_cast<const uint4 *>(sX + cm_off(t, c0 + 16 * j, kP));
+                const uint4 x1 = *reinterpret_cast<const uint4 *>(sX + cm_off(t, c0 + 16 * j + 8, kP));
+                const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    yv[2 * i] = fmaf(Dh, bf16lo(xw[i]), fmaf(ft, zv[2 * i], yv[2 * i]));
+                    yv[2 * i + 1] = fmaf(Dh, bf16hi(xw[i]), fmaf(ft, zv[2 * i + 1], yv[2 * i + 1]));
+                }
+                store16(dst + 16 * j, yv);
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float v[16];
+                tmem_ld16(trow + kColS + c0 + 16 * j, v);
+                put_state16(sHh, sHl, t, c0 + 16 * j, v);
+            }
+        }
+    }
+    cp_async_wait<0>();  // nothing left in flight if a wait gave up
+
+    if (p.h_last) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float v[16];
+            tmem_ld16(trow + kColS + c0 + 16 * j, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                p.h_last[st_base + (long long)(c0 + 16 * j + i) * kN + r] = v[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+template <typename Tout>
+int ssd_tc_t(const ssh::SsdParams &p, cudaStream_t st) {
+    const int smem = (int)sizeof(TcSmem) + 128;
+    auto kern = ssd_tc_kernel<Tout>;
+    static bool done[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
+    if (!done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return SS_ERR_CUDA;
+        done[dev] = true;
+    }
+    kern<<<(unsigned)((long long)p.batch * p.heads), kThreads, smem, st>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+}  // namespace
+
+bool ssh::ssd_tc_supported(const ssh::SsdParams &p) {
+    return p.in_dtype == SS_BF16 && p.headdim == kP && p.dstate == kN && p.seqlen % kQ == 0 &&
+           (long long)p.batch * p.heads < (1LL << 31);
+}
+
+int ssh::launch_ssd_tc(const ssh::SsdParams &p, cudaStream_t st) {
+    if (!ssd_tc_supported(p)) return SS_ERR_UNSUPPORTED;
+    return p.out_dtype == SS_BF16 ? ssd_tc_t<uint16_t>(p, st) : ssd_tc_t<float>(p, st);
+}

@@ -33,7 +33,33 @@ def _case(seed, batch, L, H, N, P=64):
                 bits=dict(x=x_bits, dt=dt_bits, B=B_bits, C=C_bits))
 
 
-def _oracle(c, batch, L, H, N, P=64, with_h0=True):
+def _sub(c, b, h):
+    """The case restricted to batch b and head h (heads are independent)."""
+    bits = c["bits"]
+    return dict(x=c["x"][b:b + 1, :, h:h + 1], dt=c["dt"][b:b + 1, :, h:h + 1],
+                B=c["B"][b:b + 1], C=c["C"][b:b + 1], A=c["A"][h:h + 1], D=c["D"][h:h + 1],
+                bias=c["bias"][h:h + 1], h0=c["h0"][b:b + 1, h:h + 1],
+                bits=dict(x=bits["x"][b:b + 1, :, h:h + 1], dt=bits["dt"][b:b + 1, :, h:h + 1],
+                          B=bits["B"][b:b + 1], C=bits["C"][b:b + 1]))
+
+
+def _ctx(path):
+    ctx = ss.Context()
+    ctx.set_option(ss.SS_OPT_SSD_PATH, path)
+    return ctx
+
+
+def _run(c, ctx, with_h0=True, **kw):
+    cu = lambda t: t.cuda()
+    y, hl = ss.ss_ssd_fwd(cu(c["x"]), cu(c["dt"]), torch.from_numpy(c["A"]).cuda(), cu(c["B"]),
+                          cu(c["C"]), D=torch.from_numpy(c["D"]).cuda(),
+                          dt_bias=torch.from_numpy(c["bias"]).cuda(),
+                          h0=torch.from_numpy(c["h0"]).cuda() if with_h0 else None, ctx=ctx, **kw)
+    torch.cuda.synchronize()
+    return y, hl
+
+
+def _oracle(c, batch, L, H, N, P=64, with_h0=True, softplus=True):
     """The same computation as an ss_scan over d = h*P + p channels."""
     bits = c["bits"]
     u = bits["x"].transpose(0, 2, 3, 1).reshape(batch, H * P, L)          # (b, d, l)
@@ -44,24 +70,65 @@ def _oracle(c, batch, L, H, N, P=64, with_h0=True):
     h0 = c["h0"].reshape(batch, H * P, N).astype(np.float64) if with_h0 else None
     y, hl = oracle.scan_fwd(np.ascontiguousarray(u), np.ascontiguousarray(delta), A, Bs, Cs,
                             D=np.repeat(c["D"], P), delta_bias=np.repeat(c["bias"], P), z=None,
-                            h0=h0)
+                            h0=h0, delta_softplus=softplus)
     return (y.reshape(batch, H, P, L).transpose(0, 3, 1, 2), hl.reshape(batch, H, P, N))
 
 
 @pytest.mark.parametrize("batch,L,H,N", [(2, 128, 3, 64), (1, 256, 2, 128), (2, 64, 1, 128),
-                                         (1, 1024, 2, 128)])
+                                         (1, 1024, 2, 128), (3, 384, 5, 128)])
 @pytest.mark.parametrize("with_h0", [True, False])
-def test_ssd_matches_scan_oracle(batch, L, H, N, with_h0):
+@pytest.mark.parametrize("path", ["auto", "tcgen05"])
+def test_ssd_matches_scan_oracle(batch, L, H, N, with_h0, path):
+    """Both kernels: the mma.sync one (the default) and the tensor-memory one
+    (dstate 128, seqlen % 128 == 0; other shapes are refused)."""
     c = _case(200 + L + N + H, batch, L, H, N)
-    cu = lambda t: t.cuda()
-    y, hl = ss.ss_ssd_fwd(cu(c["x"]), cu(c["dt"]), torch.from_numpy(c["A"]).cuda(), cu(c["B"]),
-                          cu(c["C"]), D=torch.from_numpy(c["D"]).cuda(),
-                          dt_bias=torch.from_numpy(c["bias"]).cuda(),
-                          h0=torch.from_numpy(c["h0"]).cuda() if with_h0 else None)
-    torch.cuda.synchronize()
+    tc = path == "tcgen05"
+    ctx = _ctx(ss.SS_SSD_PATH_TCGEN05 if tc else ss.SS_SSD_PATH_AUTO)
+    if tc and not (N == 128 and L % 128 == 0):
+        with pytest.raises(ss.SSError) as ei:
+            _run(c, ctx, with_h0)
+        assert ei.value.status == ss.SS_ERR_UNSUPPORTED
+        return
+    y, hl = _run(c, ctx, with_h0)
+    assert ctx.last_launch()[0] == (1 if tc else 0)
     y_ref, h_ref = _oracle(c, batch, L, H, N, with_h0=with_h0)
     check_close(y.cpu().numpy(), y_ref, True, "y")
     check_close(hl.cpu().numpy(), h_ref, True, "h_last")
+
+
+def test_ssd_tensor_memory_bf16_output_and_no_softplus():
+    """Tensor-memory kernel with bf16 y, and with dt taken as is (positive)."""
+    batch, L, H, N = 2, 256, 3, 128
+    c = _case(215, batch, L, H, N)
+    ctx = _ctx(ss.SS_SSD_PATH_TCGEN05)
+    y, hl = _run(c, ctx, out_dtype=torch.bfloat16)
+    assert ctx.last_launch()[0] == 1
+    y_ref, h_ref = _oracle(c, batch, L, H, N)
+    check_close(y.float().cpu().numpy(), y_ref, True, "y bf16")
+    check_close(hl.cpu().numpy(), h_ref, True, "h_last")
+    g = np.random.default_rng(216)
+    dt, dt_bits = _bf16(np.abs(g.standard_normal((batch, L, H))) * 0.05 + 0.01)
+    c2 = dict(c, dt=dt, bias=np.zeros(H, np.float32), bits=dict(c["bits"], dt=dt_bits))
+    y, hl = _run(c2, ctx, dt_softplus=False)
+    assert ctx.last_launch()[0] == 1
+    y_ref, h_ref = _oracle(c2, batch, L, H, N, softplus=False)
+    check_close(y.cpu().numpy(), y_ref, True, "y no softplus")
+    check_close(hl.cpu().numpy(), h_ref, True, "h_last no softplus")
+
+
+def test_ssd_full_size_sampled_heads():
+    """The Mamba-2 block shape (8, 2048, 80 heads x 64, dstate 128) in one call;
+    a few (batch, head) pairs against the oracle (heads are independent)."""
+    batch, L, H, N = 8, 2048, 80, 128
+    c = _case(217, batch, L, H, N)
+    refs = {bh: _oracle(_sub(c, *bh), 1, L, 1, N) for bh in ((0, 0), (3, 41), (7, 79))}
+    for path, variant in ((ss.SS_SSD_PATH_AUTO, 0), (ss.SS_SSD_PATH_TCGEN05, 1)):
+        ctx = _ctx(path)
+        y, hl = _run(c, ctx)
+        assert ctx.last_launch()[0] == variant
+        for (b, h), (y_ref, h_ref) in refs.items():
+            check_close(y[b:b + 1, :, h:h + 1].cpu().numpy(), y_ref, True, "y (%d, %d)" % (b, h))
+            check_close(hl[b:b + 1, h:h + 1].cpu().numpy(), h_ref, True, "h_last (%d, %d)" % (b, h))
 
 
 def test_ssd_bf16_output():
