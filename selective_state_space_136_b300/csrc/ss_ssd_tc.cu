@@ -39,7 +39,7 @@ constexpr int kQ = 128;  // chunk length = MMA rows
 constexpr int kP = 64;   // head dimension
 constexpr int kN = 128;  // state size
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColG = 0;    // G (128 columns); then Z (64)
+constexpr uint32_t kColG = 0;    // G (128 columns); then Z (C H_hi in 64, C H_lo in 64)
 constexpr uint32_t kColY = 128;  // Y (64)
 constexpr uint32_t kColS = 192;  // carried state S (64)
 
@@ -49,8 +49,8 @@ struct TcSmem {
     uint16_t M[kQ * kQ];     // masked G [t][s], K-major for Y
     uint16_t X[kQ * kP];     // x of the chunk [s][p], MN-major for Y
     uint16_t Xs[kQ * kP];    // scaled x [s][p], MN-major for S
-    uint16_t Hh[kN * kP];    // carried state, high bf16 part [n][p], MN-major for Z
-    uint16_t Hl[kN * kP];    // carried state, low part (S - hi)
+    uint16_t H[kN * 2 * kP];  // carried state [n][hi p | lo p]: bf16 high part, then S - hi;
+                              // MN-major B of one 128-column Z product
     float dt[kQ];
     float cum[kQ];
     uint64_t bar;
@@ -78,7 +78,8 @@ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 constexpr uint32_t kIdG = idesc_bf16(kQ, kQ, 0, 0);  // G: C (K-major) x B (K-major)
-constexpr uint32_t kIdY = idesc_bf16(kQ, kP, 0, 1);  // Y, Z: K-major A x MN-major B
+constexpr uint32_t kIdY = idesc_bf16(kQ, kP, 0, 1);      // Y: K-major A x MN-major B
+constexpr uint32_t kIdZ = idesc_bf16(kQ, 2 * kP, 0, 1);  // Z: C x [H_hi | H_lo]
 constexpr uint32_t kIdS = idesc_bf16(kN, kP, 1, 1);  // S: B^T (MN-major) x Xs (MN-major)
 // descriptor offsets (bytes)
 constexpr uint32_t kKmLbo = 128, kKmSbo = 128 * (kQ / 8);  // K-major 128-column tiles
@@ -124,6 +125,42 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 2 x 16 fp32 columns of this thread's TMEM lane with one wait for all.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t a0, uint32_t a1, float (&v0)[16], float (&v1)[16]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(a0), "r"(a1)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v0[i] = __uint_as_float(r[0 + i]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v1[i] = __uint_as_float(r[16 + i]);
+}
+// 4 x 16 fp32 columns of this thread's TMEM lane with one wait for all.
+__device__ __forceinline__ void tmem_ld16x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, float (&v0)[16], float (&v1)[16], float (&v2)[16], float (&v3)[16]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%65];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%66];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%67];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v0[i] = __uint_as_float(r[0 + i]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v1[i] = __uint_as_float(r[16 + i]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v2[i] = __uint_as_float(r[32 + i]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v3[i] = __uint_as_float(r[48 + i]);
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
@@ -149,9 +186,8 @@ __device__ __forceinline__ float round_bf16(float v) {
     return __bfloat162float(__float2bfloat16_rn(v));
 }
 
-// Row n of the state (16 columns at p0) as bf16 hi and lo parts into Hh / Hl.
-__device__ __forceinline__ void put_state16(uint8_t *hh, uint8_t *hl, int n, int p0,
-                                            const float (&v)[16]) {
+// Row n of the state (16 columns at p0) as bf16 hi and lo parts into the H tile.
+__device__ __forceinline__ void put_state16(uint8_t *hs, int n, int p0, const float (&v)[16]) {
     uint32_t wh[8], wl[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -159,10 +195,19 @@ __device__ __forceinline__ void put_state16(uint8_t *hh, uint8_t *hl, int n, int
         wh[j] = pack2(h0, h1);
         wl[j] = pack2(v[2 * j] - h0, v[2 * j + 1] - h1);
     }
-    *reinterpret_cast<uint4 *>(hh + cm_off(n, p0, kP)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-    *reinterpret_cast<uint4 *>(hh + cm_off(n, p0 + 8, kP)) = make_uint4(wh[4], wh[5], wh[6], wh[7]);
-    *reinterpret_cast<uint4 *>(hl + cm_off(n, p0, kP)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-    *reinterpret_cast<uint4 *>(hl + cm_off(n, p0 + 8, kP)) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+    constexpr int W = 2 * kP;
+    *reinterpret_cast<uint4 *>(hs + cm_off(n, p0, W)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+    *reinterpret_cast<uint4 *>(hs + cm_off(n, p0 + 8, W)) = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+    *reinterpret_cast<uint4 *>(hs + cm_off(n, kP + p0, W)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    *reinterpret_cast<uint4 *>(hs + cm_off(n, kP + p0 + 8, W)) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+}
+
+// Bounded wait for an MMA commit: polls mbarrier.try_wait (which itself
+// suspends for a while) without sleeping in between.
+__device__ __forceinline__ bool mma_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
 }
 
 __device__ __forceinline__ void store16(float *dst, const float (&v)[16]) {
@@ -188,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     uint8_t *sM = reinterpret_cast<uint8_t *>(sm.M), *sX = reinterpret_cast<uint8_t *>(sm.X);
     uint8_t *sXs = reinterpret_cast<uint8_t *>(sm.Xs);
-    uint8_t *sHh = reinterpret_cast<uint8_t *>(sm.Hh), *sHl = reinterpret_cast<uint8_t *>(sm.Hl);
+    uint8_t *sH = reinterpret_cast<uint8_t *>(sm.H);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
@@ -272,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
     const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);  // this warp's lanes
     const int c0 = 32 * half;  // this thread's columns of Y, Z and S
 
-    // initial state: row n = r, columns [c0, c0 + 32) of S (tensor memory) and Hh / Hl
+    // initial state: row n = r, columns [c0, c0 + 32) of S (tensor memory) and of H
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         float v[16];
@@ -280,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         for (int i = 0; i < 16; ++i)
             v[i] = p.h0 ? p.h0[st_base + (long long)(c0 + 16 * j + i) * kN + r] : 0.f;
         tmem_st16(trow + kColS + c0 + 16 * j, v);
-        put_state16(sHh, sHl, r, c0 + 16 * j, v);
+        put_state16(sH, r, c0 + 16 * j, v);
     }
     tmem_wait_st();
 
@@ -357,17 +402,15 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
                 *reinterpret_cast<uint4 *>(sXs + cm_off(s, 8 * p8, kP)) = o;
             }
             const float dec = ex2(cum_last);
+            float v0[16], v1[16];
+            tmem_ld16x2(trow + kColS + c0, trow + kColS + c0 + 16, v0, v1);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float v[16];
-                tmem_ld16(trow + kColS + c0 + 16 * j, v);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] *= dec;
-                tmem_st16(trow + kColS + c0 + 16 * j, v);
-            }
+            for (int i = 0; i < 16; ++i) v0[i] *= dec, v1[i] *= dec;
+            tmem_st16(trow + kColS + c0, v0);
+            tmem_st16(trow + kColS + c0 + 16, v1);
             tmem_wait_st();
         }
-        if (__syncthreads_or(!mbar_wait_bounded(&sm.bar, phase, p.wait_limit))) {
+        if (__syncthreads_or(!mma_wait(&sm.bar, phase, p.wait_limit))) {
             if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
             break;
         }
@@ -379,10 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         {
             const int t = r;
             const float ct = sm.cum[t];
-            for (int j = half; j < 2 * (quarter + 1); j += 2) {
-                const int s0 = 16 * j;
-                float g[16];
-                tmem_ld16(trow + kColG + s0, g);
+            // this warp's pieces j = half, half + 2, ... (quarter + 1 of them), two per load
+            auto mask_piece = [&](int s0, const float (&g)[16]) {
                 uint32_t w[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -395,6 +436,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
                 *reinterpret_cast<uint4 *>(sM + cm_off(t, s0, kQ)) = make_uint4(w[0], w[1], w[2], w[3]);
                 *reinterpret_cast<uint4 *>(sM + cm_off(t, s0 + 8, kQ)) =
                     make_uint4(w[4], w[5], w[6], w[7]);
+            };
+            for (int k = 0; k <= quarter; k += 2) {
+                const int s0 = 16 * (half + 2 * k);
+                if (k + 1 <= quarter) {
+                    float g0[16], g1[16];
+                    tmem_ld16x2(trow + kColG + s0, trow + kColG + s0 + 32, g0, g1);
+                    mask_piece(s0, g0);
+                    mask_piece(s0 + 32, g1);
+                } else {
+                    float g0[16];
+                    tmem_ld16(trow + kColG + s0, g0);
+                    mask_piece(s0, g0);
+                }
             }
         }
         fence_proxy_async();
@@ -402,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         __syncthreads();
         tc_fence_after();
 
-        // ---- Y = M X, Z = C (Hh + Hl) (into G's columns), S += B^T Xs
+        // ---- Y = M X, Z = C [H_hi | H_lo] (into G's columns), S += B^T Xs
         if (tid == 0) {
 #pragma unroll
             for (int k = 0; k < kQ / 16; ++k)
@@ -411,18 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
 #pragma unroll
             for (int k = 0; k < kN / 16; ++k)
                 mma_f16(tmem + kColG, sdesc(sC, k * kKmStep, kKmLbo, kKmSbo),
-                        sdesc(sHh, k * kMn64Step, kMn64Lbo, kMn64Sbo), kIdY, k > 0);
-#pragma unroll
-            for (int k = 0; k < kN / 16; ++k)
-                mma_f16(tmem + kColG, sdesc(sC, k * kKmStep, kKmLbo, kKmSbo),
-                        sdesc(sHl, k * kMn64Step, kMn64Lbo, kMn64Sbo), kIdY, true);
+                        sdesc(sH, k * kMn128Step, kMn128Lbo, kMn128Sbo), kIdZ, k > 0);
 #pragma unroll
             for (int k = 0; k < kQ / 16; ++k)
                 mma_f16(tmem + kColS, sdesc(sB, k * kMn128Step, kMn128Lbo, kMn128Sbo),
                         sdesc(sXs, k * kMn64Step, kMn64Lbo, kMn64Sbo), kIdS, true);
             mma_commit(&sm.bar);
         }
-        if (__syncthreads_or(!mbar_wait_bounded(&sm.bar, phase, p.wait_limit))) {
+        if (__syncthreads_or(!mma_wait(&sm.bar, phase, p.wait_limit))) {
             if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
             break;
         }
@@ -430,45 +480,45 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         tc_fence_after();
 
         // ---- y row t = r, this half's 32 channels; the new state's row n = r
-        // (same columns) into Hh / Hl
+        // (same columns) into H
         {
             const int t = r;
             const float ft = ex2(sm.cum[t]);
             Tout *dst = static_cast<Tout *>(p.y) + ((long long)b * L + l0 + t) * xs_t +
                         (long long)h * kP + c0;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float yv[16], zv[16];
-                tmem_ld16(trow + kColY + c0 + 16 * j, yv);
-                tmem_ld16(trow + kColG + c0 + 16 * j, zv);
+            float y0[16], y1[16], zh0[16], zh1[16], zl0[16], zl1[16];
+            tmem_ld16x4(trow + kColY + c0, trow + kColY + c0 + 16, trow + kColG + c0,
+                        trow + kColG + c0 + 16, y0, y1, zh0, zh1);
+            tmem_ld16x2(trow + kColG + kP + c0, trow + kColG + kP + c0 + 16, zl0, zl1);
+            auto finish = [&](int j, float (&yv)[16], const float (&zh)[16], const float (&zl)[16]) {
                 const uint4 x0 = *reinterpret_cast<const uint4 *>(sX + cm_off(t, c0 + 16 * j, kP));
                 const uint4 x1 = *reinterpret_cast<const uint4 *>(sX + cm_off(t, c0 + 16 * j + 8, kP));
                 const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    yv[2 * i] = fmaf(Dh, bf16lo(xw[i]), fmaf(ft, zv[2 * i], yv[2 * i]));
-                    yv[2 * i + 1] = fmaf(Dh, bf16hi(xw[i]), fmaf(ft, zv[2 * i + 1], yv[2 * i + 1]));
+                    yv[2 * i] = fmaf(Dh, bf16lo(xw[i]), fmaf(ft, zh[2 * i] + zl[2 * i], yv[2 * i]));
+                    yv[2 * i + 1] = fmaf(Dh, bf16hi(xw[i]),
+                                         fmaf(ft, zh[2 * i + 1] + zl[2 * i + 1], yv[2 * i + 1]));
                 }
                 store16(dst + 16 * j, yv);
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float v[16];
-                tmem_ld16(trow + kColS + c0 + 16 * j, v);
-                put_state16(sHh, sHl, t, c0 + 16 * j, v);
-            }
+            };
+            finish(0, y0, zh0, zl0);
+            finish(1, y1, zh1, zl1);
+            float v0[16], v1[16];
+            tmem_ld16x2(trow + kColS + c0, trow + kColS + c0 + 16, v0, v1);
+            put_state16(sH, t, c0, v0);
+            put_state16(sH, t, c0 + 16, v1);
         }
     }
     cp_async_wait<0>();  // nothing left in flight if a wait gave up
 
     if (p.h_last) {
+        float v0[16], v1[16];
+        tmem_ld16x2(trow + kColS + c0, trow + kColS + c0 + 16, v0, v1);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            float v[16];
-            tmem_ld16(trow + kColS + c0 + 16 * j, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                p.h_last[st_base + (long long)(c0 + 16 * j + i) * kN + r] = v[i];
+        for (int i = 0; i < 16; ++i) {
+            p.h_last[st_base + (long long)(c0 + i) * kN + r] = v0[i];
+            p.h_last[st_base + (long long)(c0 + 16 + i) * kN + r] = v1[i];
         }
     }
     tc_fence_before();
