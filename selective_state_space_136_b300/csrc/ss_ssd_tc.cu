@@ -177,6 +177,21 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Global loads kept in program order (volatile): issued where written, one
+// chunk ahead of their use, rather than moved next to it.
+__device__ __forceinline__ uint4 ldg_v4_ordered(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint16_t ldg_u16_ordered(const void *p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
     const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
@@ -272,16 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
 #pragma unroll
         for (int k = 0; k < kXPieces; ++k) {
             const int i = tid + kThreads * k, s = i % kQ, p8 = i / kQ;
-            xr[k] = __ldg(reinterpret_cast<const uint4 *>(
-                gx + ((long long)b * L + l0 + s) * xs_t + (long long)h * kP + 8 * p8));
+            xr[k] = ldg_v4_ordered(gx + ((long long)b * L + l0 + s) * xs_t + (long long)h * kP + 8 * p8);
         }
     };
     // raw dt of chunk c, four steps per lane of warp 0
-    auto load_dt = [&](int c, float (&dr)[4]) {
+    auto load_dt = [&](int c, uint16_t (&dr)[4]) {
         const long long l0 = (long long)c * kQ;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            dr[k] = to_f32(gdt[((long long)b * L + l0 + 4 * lane + k) * p.heads + h]);
+            dr[k] = ldg_u16_ordered(gdt + ((long long)b * L + l0 + 4 * lane + k) * p.heads + h);
     };
 
     if (warp == 0) {
@@ -304,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
             *reinterpret_cast<uint4 *>(sM + cm_off(t, 8 * s8, kQ)) = make_uint4(0u, 0u, 0u, 0u);
     }
     uint4 xr[kXPieces];
-    float dr[4] = {0.f, 0.f, 0.f, 0.f};
+    uint16_t dr[4] = {0, 0, 0, 0};
     if (n_chunks > 0) {
         issue_cb(0);
         load_x(0, xr);
@@ -345,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
             float d4[4], c4[4], run = 0.f;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float xv = dr[k] + bias;
+                const float xv = to_f32(dr[k]) + bias;
                 d4[k] = p.softplus ? softplus1(xv) : xv;
                 run += d4[k] * a;
                 c4[k] = run;
