@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
     tmem_wait_st();
 
     uint32_t phase = 0;
+    bool timed_out = false;
     for (int c = 0; c < n_chunks; ++c) {
         const long long l0 = (long long)c * kQ;
         const uint8_t *sC = reinterpret_cast<const uint8_t *>(sm.C[c & 1]);
@@ -426,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         }
         if (__syncthreads_or(!mma_wait(&sm.bar, phase, p.wait_limit))) {
             if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
+            timed_out = true;
             break;
         }
         phase ^= 1u;
@@ -488,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         }
         if (__syncthreads_or(!mma_wait(&sm.bar, phase, p.wait_limit))) {
             if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
+            timed_out = true;
             break;
         }
         phase ^= 1u;
@@ -525,6 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         }
     }
     cp_async_wait<0>();  // nothing left in flight if a wait gave up
+    // after a wait that gave up, give the committed products one more bounded
+    // wait before their tensor memory is freed
+    if (timed_out) mma_wait(&sm.bar, phase, p.wait_limit);
 
     if (p.h_last) {
         float v0[16], v1[16];
