@@ -654,7 +654,8 @@ def run_ours(args, rank, world, local):
     bdln = elements * cfg.dstate
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     terms = {"hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "peak_source": hbm_src,
-                     "floor_us": nbytes / (hbm_peak * 1e9) * 1e6}}
+                     "floor_us": nbytes / (hbm_peak * 1e9) * 1e6,
+                     "frac_of_nominal_8000": gbs / 8000.0}}
     fp32_peak = sms * FP32_LANES_PER_SM * MAX_SM_MHZ * 1e6 / 1e12     # Tops/s
     fp32_ops = 4.0 * bdln
     terms["fp32"] = {"achieved": fp32_ops / avg_launch_s / 1e12, "peak": fp32_peak,
@@ -666,10 +667,15 @@ def run_ours(args, rank, world, local):
         per_clk = probes["ex2"]["ops_per_s"] / (sms * probes["ex2"]["sm_ghz"] * 1e9)
         per_clk_arch = float(2 ** round(np.log2(max(per_clk, 1e-9))))
         ex2_peak = sms * per_clk_arch * MAX_SM_MHZ * 1e6 / 1e9            # Gex2/s
+        # all MUFU work of the call: the N decays per element plus softplus (2) and
+        # the gate (2) per (b, d, l)
+        mufu_all = elements * (cfg.dstate + 4)
         terms["ex2"] = {"achieved": bdln / avg_launch_s / 1e9, "peak": ex2_peak,
                         "unit": "Gex2/s", "floor_us": bdln / (ex2_peak * 1e9) * 1e6,
                         "ex2_per_clk_per_sm_measured": per_clk,
-                        "ex2_per_clk_per_sm_used": per_clk_arch}
+                        "ex2_per_clk_per_sm_used": per_clk_arch,
+                        "mufu_all_ops": mufu_all,
+                        "mufu_all_floor_us": mufu_all / (ex2_peak * 1e9) * 1e6}
     for t in terms.values():
         t["frac"] = t["achieved"] / t["peak"]
     dominant = max(terms, key=lambda k: terms[k]["floor_us"])
