@@ -70,6 +70,25 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def max_over_ranks(pg, value, device):
+    """The largest of every rank's `value` (a job's timed region lasts as long
+    as its slowest rank's); `value` itself when there is one rank (pg None).
+    `pg` is torch.distributed with any backend; `device` is where that
+    backend's tensors live (a GPU for NCCL, the CPU for gloo)."""
+    if pg is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, units_per_rank, steps, max_ms):
+    """Whole-job units per second: every rank processed `units_per_rank` per
+    step (replicas, weak scaling) within the slowest rank's `max_ms`."""
+    return world * units_per_rank * steps / (max_ms * 1e-3)
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -557,13 +576,10 @@ def run_ours(args, rank, world, local):
     total_ms = ev[0].elapsed_time(ev[-1])
     if ctx.device_error() != ss.SS_OK:
         raise RuntimeError("device error in the timed region")
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(pg, total_ms, dev)
 
     elements = cfg.elements
-    value = world * elements * args.steps / (total_ms * 1e-3)
+    value = replica_throughput(world, elements, args.steps, total_ms)
     ms_per_step = total_ms / args.steps
     # one call = the whole path (B/C pack + scan); the scan kernel is ~99% of it
     avg_launch_s = float(np.mean(per_launch_ms)) * 1e-3
@@ -632,11 +648,8 @@ def run_ours(args, rank, world, local):
             e2e_step(k)
         torch.cuda.synchronize(dev)
         e_ms = (time.perf_counter() - t0) * 1e3
-        if pg:
-            t = torch.tensor([e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * elements * k_e2e / (e_ms * 1e-3), "unit": "elements/s",
+        e_ms = max_over_ranks(pg, e_ms, dev)
+        e2e = {"value": replica_throughput(world, elements, k_e2e, e_ms), "unit": "elements/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k_e2e,
                "note": "pinned host buffers; wall clock around the steps with a synchronize on "
                        "both sides; inputs of step k+1 copied in while step k computes and "
