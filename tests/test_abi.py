@@ -61,6 +61,24 @@ def test_struct_layout_matches_binding(built, tmp_path):
     assert seen == set(structs)
 
 
+def test_enum_constants_match_binding(tmp_path):
+    """Every enumerator the header defines has the same value in the binding."""
+    import selective_state_space_136_b300 as ss
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    names = sorted(set(re.findall(r"\b(SS_[A-Z0-9_]+)\s*=", text)))
+    assert {"SS_OK", "SS_OPT_SSD_PATH", "SS_SSD_PATH_TCGEN05", "SS_DISC_ZOH"} <= set(names)
+    prog = tmp_path / "enums.c"
+    prog.write_text("\n".join(['#include <stdio.h>', '#include "ss_scan.h"', "int main(void){"] +
+                              ['printf("%s %%d\\n", (int)%s);' % (n, n) for n in names] +
+                              ["return 0;}"]))
+    exe = tmp_path / "enums"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(prog)])
+    for line in subprocess.check_output([str(exe)]).decode().split("\n"):
+        if line:
+            name, val = line.split()
+            assert getattr(ss, name) == int(val), name
+
+
 def test_host_validation_without_gpu(built):
     import selective_state_space_136_b300 as ss
     L = ss.lib()
