@@ -88,6 +88,7 @@ def test_host_validation_without_gpu(built):
     assert L.ss_scan_bwd(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_ssd_fwd(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_conv1d_update(None, None, None) == ss.SS_ERR_INVALID_ARG
+    assert L.ss_scan_fwd_noalloc(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_set_option(None, 0, 0) == ss.SS_ERR_INVALID_ARG
     assert L.ss_destroy(None) == ss.SS_OK
     assert ss.status_string(ss.SS_ERR_TIMEOUT) == "device wait timed out"
