@@ -284,9 +284,13 @@ int ss_conv1d_update(ss_ctx *ctx, const ss_conv1d_update_args *args, ss_stream_t
  *                  may be NULL.
  * The scratch array is shared by every call on a device and keeps the last
  * call's contents; the call clears what must start at zero. Calls that
- * overlap on the GPU race on it: order them on one stream. The first call on
- * a device resolves the array's address and clears it synchronously: make it
- * before any stream capture. Returns SS_OK or an error from ss_status.
+ * overlap on the GPU race on it: order them on one stream. Calls from several
+ * host threads are serialised by a per-device lock held while the call is
+ * numbered and enqueued, so on one stream they run in that order. The first
+ * successful call on a device resolves the array's address and clears it
+ * synchronously: make it before any stream capture. If that set-up fails the
+ * call returns SS_ERR_CUDA and the next call tries it again. Returns SS_OK or
+ * an error from ss_status.
  */
 int ss_scan_fwd_noalloc(const ss_scan_args *args, int *device_error, ss_stream_t stream);
 

@@ -227,12 +227,17 @@ def conv1d_update(state, x, weight, bias=None, silu=False, dim=None):
 
 
 def scan_bwd(u, delta, A, B, C, dy, D=None, delta_bias=None, z=None, delta_softplus=True,
-             h0=None, dh_last=None, zoh=False):
+             h0=None, dh_last=None, zoh=False, threads=1):
     """Gradients of the selective scan in fp64 (full tensors only).
 
     Same inputs as scan_fwd plus dy (batch, dim, L) and optional dh_last
     (batch, dim, N). Returns a dict with du, ddelta, dz (None without z), dA,
-    dB, dC, dD, ddelta_bias and dh0, all float64."""
+    dB, dC, dD, ddelta_bias and dh0, all float64.
+
+    threads > 1 splits the rows into that many contiguous groups, each run by
+    the same C routine on its own rows with its own buffers for the sums over
+    rows (dA, dB, dC, dD, ddelta_bias), which are added afterwards: only the
+    order of those fp64 additions changes."""
     u = np.ascontiguousarray(u)
     batch, dim, L = u.shape
     B = np.ascontiguousarray(B)
@@ -255,12 +260,35 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, delta_bias=None, z=None, delta_softp
                dz=np.zeros((batch, dim, L)) if z is not None else None,
                dA=np.zeros((dim, N)), dB=np.zeros((batch, N, L)), dC=np.zeros((batch, N, L)),
                dD=np.zeros(dim), ddelta_bias=np.zeros(dim), dh0=np.zeros((batch, dim, N)))
-    rc = _load().ss_oracle_scan_bwd(
-        nrows, _ptr(row_b), _ptr(row_d), dim, N, L, code, _ptr(u), _ptr(delta), _ptr(z),
-        _ptr(A), _ptr(B), _ptr(C), _ptr(Dp), _ptr(bp), int(bool(delta_softplus)), _ptr(h0p),
-        int(bool(zoh)), _ptr(dyp), _ptr(dhp), _ptr(out["du"]), _ptr(out["ddelta"]),
-        _ptr(out["dz"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
-        _ptr(out["ddelta_bias"]), _ptr(out["dh0"]))
-    if rc != 0:
-        raise ValueError("oracle rejected its arguments")
+    lib = _load()
+
+    def run_rows(lo, hi):
+        """Rows [lo, hi): per-row outputs written in place, sums returned."""
+        sums = dict(dA=np.zeros((dim, N)), dB=np.zeros((batch, N, L)), dC=np.zeros((batch, N, L)),
+                    dD=np.zeros(dim), ddelta_bias=np.zeros(dim))
+        sl = lambda a, w: None if a is None else a.reshape(nrows, w)[lo:hi]
+        view = lambda a: None if a is None else a.reshape(nrows, L)[lo:hi]
+        rc = lib.ss_oracle_scan_bwd(
+            hi - lo, _ptr(row_b[lo:hi]), _ptr(row_d[lo:hi]), dim, N, L, code,
+            _ptr(view(u)), _ptr(view(delta)), _ptr(view(z)), _ptr(A), _ptr(B), _ptr(C),
+            _ptr(Dp), _ptr(bp), int(bool(delta_softplus)), _ptr(sl(h0p, N)), int(bool(zoh)),
+            _ptr(view(dyp)), _ptr(sl(dhp, N)), _ptr(view(out["du"])), _ptr(view(out["ddelta"])),
+            _ptr(view(out["dz"])), _ptr(sums["dA"]), _ptr(sums["dB"]), _ptr(sums["dC"]),
+            _ptr(sums["dD"]), _ptr(sums["ddelta_bias"]), _ptr(sl(out["dh0"], N)))
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        return sums
+
+    groups = max(1, min(int(threads), nrows))
+    bounds = [(nrows * k // groups, nrows * (k + 1) // groups) for k in range(groups)]
+    if groups == 1:
+        parts = [run_rows(0, nrows)]
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(groups) as ex:
+            parts = list(ex.map(lambda b: run_rows(*b), bounds))
+    for k in ("dA", "dB", "dC", "dD", "ddelta_bias"):
+        out[k] = parts[0][k]
+        for part in parts[1:]:
+            out[k] += part[k]
     return out

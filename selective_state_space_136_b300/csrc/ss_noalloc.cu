@@ -13,17 +13,22 @@
 // per-row-block flags, carry buffer, packed fp32 B/C) lives in one
 // file-scope __device__ array of kNoAllocScratchBytes (8 MiB). Every GPU that
 // loads this library keeps that array until the process exits. The first
-// call on a device resolves the array's device address (cudaGetSymbolAddress,
-// with that device current) and zeroes the flags once with a synchronous
-// cudaMemset; make that first call before any stream capture. Later calls
-// only enqueue kernels.
+// successful call on a device resolves the array's device address
+// (cudaGetSymbolAddress, with that device current) and zeroes the flags once
+// with a synchronous cudaMemset; make that first call before any stream
+// capture. A set-up that fails is retried by the next call. Later calls only
+// enqueue kernels.
 //
 // Every call on a device shares the one array and leaves its contents behind:
 // the work counter is reset by the first kernel of each call and the flags are
-// tagged with a per-device call number, so stale contents are never read. Two
-// calls that overlap on the GPU (different streams, no ordering between them)
-// race on the array and give wrong results; order them on one stream.
-#include <functional>
+// tagged with a per-device call number, so stale contents are never read. The
+// call number is drawn and the kernels are enqueued under one per-device lock,
+// so calls from several host threads on one stream run in call-number order
+// (the calls are serialised on the host). A chained wait accepts only its own
+// call's flag: a flag left by any other call makes it give up after its
+// bounded wait and report SS_ERR_TIMEOUT instead of reading a foreign carry.
+// Two calls that overlap on the GPU (different streams, no ordering between
+// them) race on the array and give wrong results; order them on one stream.
 #include <mutex>
 
 #include "ss_internal.h"
@@ -36,12 +41,11 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 struct DeviceSlot {
-    std::once_flag once;
-    int status = SS_ERR_CUDA;  // result of the one-time set-up
+    bool ready = false;  // set-up done (only ever set on success)
     unsigned char *base = nullptr;
     unsigned long long calls = 0;
     int sm_count = 0;
-    std::mutex mu;  // guards `calls`
+    std::mutex mu;  // guards the set-up, `calls` and the enqueue of a call
 };
 DeviceSlot g_slots[kMaxDevices];
 
@@ -55,17 +59,21 @@ size_t scratch_need(const ssh::ScanParams &p, size_t *flags_b, size_t *carry_b) 
     return 256 + *flags_b + *carry_b + up256(ssh::pair_bc_bytes(p));
 }
 
-void setup(int dev, DeviceSlot &slot) {
+// One-time set-up of a device's slot, called with slot.mu held and the device
+// current; on failure the slot stays not ready and the next call tries again.
+int setup(int dev, DeviceSlot &slot) {
     void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return;
-    if (cudaDeviceGetAttribute(&slot.sm_count, cudaDevAttrMultiProcessorCount, dev) !=
-        cudaSuccess)
-        return;
+    int sms = 0;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SS_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SS_ERR_CUDA;
     // flags must start below every call number; nothing else needs clearing
-    if (cudaMemset(ptr, 0, kNoAllocScratchBytes) != cudaSuccess) return;
-    if (cudaDeviceSynchronize() != cudaSuccess) return;
+    if (cudaMemset(ptr, 0, kNoAllocScratchBytes) != cudaSuccess) return SS_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SS_ERR_CUDA;
     slot.base = static_cast<unsigned char *>(ptr);
-    slot.status = SS_OK;
+    slot.sm_count = sms;
+    slot.ready = true;
+    return SS_OK;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -116,18 +124,19 @@ extern "C" int ss_scan_fwd_noalloc(const ss_scan_args *a, int *device_error,
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SS_ERR_CUDA;
     DeviceSlot &slot = g_slots[dev];
-    std::call_once(slot.once, setup, dev, std::ref(slot));
-    if (slot.status != SS_OK) return slot.status;
-
+    // the call number and the enqueue happen under one lock, so the kernels of
+    // calls made from several threads reach the stream in call-number order
+    std::lock_guard<std::mutex> g(slot.mu);
+    if (!slot.ready) {
+        const int rc = setup(dev, slot);
+        if (rc != SS_OK) return rc;
+    }
     ssh::PairWork w{};
     w.counter = reinterpret_cast<unsigned long long *>(slot.base);
     w.flags = reinterpret_cast<unsigned long long *>(slot.base + 256);
     w.carry = reinterpret_cast<float *>(slot.base + 256 + flags_b);
     w.bc = reinterpret_cast<float *>(slot.base + 256 + flags_b + carry_b);
-    {
-        std::lock_guard<std::mutex> g(slot.mu);
-        w.epoch = ++slot.calls;
-    }
+    w.epoch = ++slot.calls;
     w.n_seg = 1;
     w.warps_per_sm = 8;
     w.sm_count = slot.sm_count;

@@ -346,13 +346,15 @@ __global__ void SS_PAIR_BOUNDS
                     src1 = p.h0 + ((long long)b * p.dim + dp) * kN;
                 }
             } else {
-                // the tail of a split row block: wait for its head's carry
+                // the tail of a split row block: wait for its head's carry. Only
+                // this call's flag counts: one left by another call (any other
+                // epoch) runs the bounded wait out and reports a timeout.
                 const unsigned long long want = (sch.epoch << 16) | 1ull;
                 bool ok = true;
                 if (lane == 0) {
                     ok = false;
                     for (uint32_t i = 0; i < p.wait_limit; ++i) {
-                        if (ld_acquire(sch.flags + rbi) >= want) {
+                        if (ld_acquire(sch.flags + rbi) == want) {
                             ok = true;
                             break;
                         }

@@ -99,6 +99,27 @@ def test_bwd_long_rows():
         _close(got[k], ref[k], True, k)
 
 
+def test_bwd_full_shape():
+    """The 2.8B-block shape (8, 5120, 16, 2048), bf16, every gradient: 1280 row
+    blocks in one wave and the per-step atomic sums of dB and dC over all 5120
+    channels of a batch, against the oracle run on every row (rows split over
+    the host's cores, partial sums added)."""
+    cfg = workloads.CONFIGS["mamba2p8b"]
+    inp = workloads.scan_inputs(cfg)
+    t = device_inputs(inp, cfg)
+    shp = (cfg.batch, cfg.dim, cfg.seqlen)
+    dy = np.random.default_rng(11).standard_normal(shp).astype(np.float32)
+    got = ss.ss_scan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], torch.from_numpy(dy).cuda(),
+                         D=t["D"], delta_bias=t["delta_bias"], z=t["z"])
+    torch.cuda.synchronize()
+    ref = oracle.scan_bwd(inp["u"].reshape(shp), inp["delta"].reshape(shp), inp["A"], inp["B"],
+                          inp["C"], dy.astype(np.float64), D=inp["D"],
+                          delta_bias=inp["delta_bias"], z=inp["z"].reshape(shp),
+                          threads=oracle._cpu_threads())
+    for k in ("du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias"):
+        _close(got[k], ref[k], True, k)
+
+
 def test_bwd_host_checks():
     cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=1, dim=32, seqlen=24, seed=1)
     inp = workloads.scan_inputs(cfg)

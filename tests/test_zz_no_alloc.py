@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import workloads
-from gpu_util import check_close, device_inputs
+from gpu_util import check_close, device_inputs, oracle_rows, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +55,35 @@ def test_matches_regular_entry_point_twice(lib):
         assert int(err[0].item()) == 0
         check_close(y.cpu().numpy(), y_ref.cpu().numpy(), True, "y")
         check_close(hl.cpu().numpy(), h_ref.cpu().numpy(), True, "h_last")
+
+
+def test_split_row_blocks_twice_against_oracle(lib):
+    """More row blocks (2048) than chained ranges (8 per SM), so row blocks are
+    split between two ranges and their tail pieces wait on flags in the shared
+    array; the second call must ignore the first call's flags and carries."""
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    err = torch.zeros(4, dtype=torch.int32, device="cuda")
+    for seed in (81, 82):
+        cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=8, dim=8192, seqlen=64,
+                               seed=seed)
+        inp = workloads.scan_inputs(cfg)
+        t = device_inputs(inp, cfg)
+        y_ref, h_ref = ss.ss_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"],
+                                      delta_bias=t["delta_bias"], z=t["z"])
+        y = torch.full_like(y_ref, float("nan"))
+        hl = torch.full_like(h_ref, float("nan"))
+        assert lib.ss_scan_fwd_noalloc(ctypes.byref(_args(cfg, t, y, hl)),
+                                       ctypes.c_void_p(err.data_ptr()), st) == 0
+        torch.cuda.synchronize()
+        assert int(err[0].item()) == 0
+        check_close(y.cpu().numpy(), y_ref.cpu().numpy(), True, "y vs ss_scan_fwd")
+        check_close(hl.cpu().numpy(), h_ref.cpu().numpy(), True, "h_last vs ss_scan_fwd")
+        rows = sample_rows(cfg, 64, seed=seed)
+        yo, ho = oracle_rows(inp, cfg, rows)
+        yg = y.reshape(cfg.rows, cfg.seqlen).cpu().numpy()[rows]
+        hg = hl.reshape(cfg.rows, cfg.dstate).cpu().numpy()[rows]
+        check_close(yg, yo, True, "y vs oracle")
+        check_close(hg, ho, True, "h_last vs oracle")
 
 
 def test_refuses_shapes_beyond_the_static_scratch(lib):
