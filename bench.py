@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--skip-conv", action="store_true", help="skip the conv1d leg")
     ap.add_argument("--skip-bwd", action="store_true", help="skip the backward leg")
     ap.add_argument("--skip-ssd", action="store_true", help="skip the Mamba-2 SSD leg")
+    ap.add_argument("--skip-configs", action="store_true",
+                    help="skip the mamba130m and long1m scan legs")
     return ap.parse_args()
 
 
@@ -498,6 +500,123 @@ def time_ssd(ss, ctx, dev, stream, args, batch=8, L=2048, H=80, P=64, N=128, pro
             "steps": steps, "gpu_launches": steps}
 
 
+def sms_of(dev):
+    import torch
+    return torch.cuda.get_device_properties(dev).multi_processor_count
+
+
+def scan_roofline(cfg, avg_s, probes, sms):
+    """Roofline of one ss_scan_fwd call on `cfg` taking `avg_s` seconds: the
+    HBM, FP32 and ex2 floors (max of them binds), plus the informative issue and
+    mixed-unit floors."""
+    hbm_peak, hbm_src = measured_peaks()
+    nbytes = step_bytes(cfg)
+    elements = cfg.elements
+    gbs = nbytes / avg_s / 1e9
+    bdln = elements * cfg.dstate
+    terms = {"hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "peak_source": hbm_src,
+                     "floor_us": nbytes / (hbm_peak * 1e9) * 1e6,
+                     "frac_of_nominal_8000": gbs / 8000.0}}
+    fp32_peak = sms * FP32_LANES_PER_SM * MAX_SM_MHZ * 1e6 / 1e12     # Tops/s
+    fp32_ops = 4.0 * bdln
+    terms["fp32"] = {"achieved": fp32_ops / avg_s / 1e12, "peak": fp32_peak,
+                     "unit": "Tops/s", "floor_us": fp32_ops / (fp32_peak * 1e12) * 1e6,
+                     "note": "4 FMA-pipe lane ops per state element (dt*A, dt*u*B, state FMA, "
+                             "output FMA) against %d lanes/SM at %.0f MHz" % (FP32_LANES_PER_SM,
+                                                                             MAX_SM_MHZ)}
+    if probes and probes["ex2"]["rc"] == 0 and probes["ex2"]["sm_ghz"] > 0:
+        per_clk = probes["ex2"]["ops_per_s"] / (sms * probes["ex2"]["sm_ghz"] * 1e9)
+        per_clk_arch = float(2 ** round(np.log2(max(per_clk, 1e-9))))
+        ex2_peak = sms * per_clk_arch * MAX_SM_MHZ * 1e6 / 1e9            # Gex2/s
+        # all MUFU work of the call: the N decays per element plus softplus (2) and
+        # the gate (2) per (b, d, l)
+        mufu_all = elements * (cfg.dstate + 4)
+        terms["ex2"] = {"achieved": bdln / avg_s / 1e9, "peak": ex2_peak,
+                        "unit": "Gex2/s", "floor_us": bdln / (ex2_peak * 1e9) * 1e6,
+                        "ex2_per_clk_per_sm_measured": per_clk,
+                        "ex2_per_clk_per_sm_used": per_clk_arch,
+                        "mufu_all_ops": mufu_all,
+                        "mufu_all_floor_us": mufu_all / (ex2_peak * 1e9) * 1e6}
+    for t in terms.values():
+        t["frac"] = t["achieved"] / t["peak"]
+    dominant = max(terms, key=lambda k: terms[k]["floor_us"])
+    # informative: the 4 FP32 lane-ops and the ex2 of a state element all take
+    # issue slots of the same warp scheduler (1 warp-instruction per clock per
+    # scheduler, 4 schedulers per SM), so 5 slots per 32 elements bound the
+    # arithmetic before any overhead; not part of the max above
+    issue_floor_us = bdln * 5 / 32 / (4 * sms) / (MAX_SM_MHZ * 1e6) * 1e6
+    issue_term = {"floor_us": issue_floor_us, "frac": issue_floor_us / (avg_s * 1e6),
+                  "note": "5 issue slots (4 FP32 + 1 MUFU) per 32 state elements, 4 schedulers/SM"}
+    # informative: the mixed probe runs ex2 and FFMA2 at the scan's ratio (one
+    # ex2 per four FMA lane-ops) on independent chains; its rate, scaled to the
+    # maximum clock, is what the two units deliver together
+    mixed_term = None
+    if probes and probes.get("mixed", {}).get("rc") == 0 and probes["mixed"]["sm_ghz"] > 0:
+        rate = probes["mixed"]["ops_per_s"] * (MAX_SM_MHZ * 1e-3) / probes["mixed"]["sm_ghz"]
+        per_clk = probes["mixed"]["ops_per_s"] / (sms * probes["mixed"]["sm_ghz"] * 1e9)
+        mixed_term = {"floor_us": bdln / rate * 1e6, "frac": bdln / rate / avg_s,
+                      "elements_per_clk_per_sm": per_clk,
+                      "note": "state elements (1 ex2 + 4 FMA lane-ops) per second that the "
+                              "mixed probe sustains, at the maximum clock"}
+    dt = terms[dominant]
+    floor = max(t["floor_us"] for t in terms.values())
+    return {"bound": "hbm" if dominant == "hbm" else "alu", "term": dominant,
+            "achieved": dt["achieved"], "peak": dt["peak"], "unit": dt["unit"],
+            "frac": dt["frac"], "traffic": None, "algorithmic_bytes_per_launch": nbytes,
+            "kernel_us": avg_s * 1e6, "floor_us": floor, "frac_of_floor": floor / (avg_s * 1e6),
+            "terms": terms, "issue_slots": issue_term, "mixed_units": mixed_term,
+            "peak_clock_mhz": MAX_SM_MHZ}
+
+
+def time_scan_config(ss, ctx, dev, stream, name, probes, warmup=3, steps=10):
+    """One other configuration of the scan (its own inputs, resident): time per
+    call from CUDA events on the launching stream, elements/s and its roofline."""
+    import torch
+    cfg = workloads.CONFIGS[name]
+    inp = workloads.scan_inputs(cfg)
+    shp = (cfg.batch, cfg.dim, cfg.seqlen)
+
+    def to_dev(a, shape):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).reshape(shape).to(dev)
+        return torch.from_numpy(a).reshape(shape).to(dev)
+
+    t = {k: to_dev(inp[k], shp) for k in ("u", "delta", "z")}
+    t["B"] = to_dev(inp["B"], inp["B"].shape)
+    t["C"] = to_dev(inp["C"], inp["C"].shape)
+    prm = {k: torch.from_numpy(inp[k]).to(dev) for k in ("A", "D", "delta_bias")}
+    del inp
+    y = torch.empty(shp, dtype=torch.float32, device=dev)
+    hl = torch.empty((cfg.batch, cfg.dim, cfg.dstate), dtype=torch.float32, device=dev)
+    call = ss.PreparedScan(t["u"], t["delta"], prm["A"], t["B"], t["C"], D=prm["D"],
+                           delta_bias=prm["delta_bias"], z=t["z"], y=y, h_last=hl, ctx=ctx,
+                           stream=stream)
+    if cfg.seqlen > 100000:
+        steps = max(3, steps // 2)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ctx.device_error() != ss.SS_OK:
+        raise RuntimeError("device error in the %s leg" % name)
+    variant, launches = ctx.last_launch()
+    avg_s = e0.elapsed_time(e1) / steps * 1e-3
+    rf = scan_roofline(cfg, avg_s, probes, sms_of(dev))
+    names = {0: "auto", 1: "rows", 2: "chunked", 3: "simple"}
+    return {"workload": workload_config(cfg)["workload"], "us_per_call": avg_s * 1e6,
+            "elements_per_s": cfg.elements / avg_s, "gbs": rf["terms"]["hbm"]["achieved"],
+            "variant": names.get(variant, str(variant)), "launches_per_call": launches,
+            "roofline": {k: rf[k] for k in ("bound", "term", "achieved", "peak", "unit", "frac",
+                                            "floor_us", "frac_of_floor", "terms")},
+            "steps": steps, "gpu_launches": steps * launches}
+
+
 def run_ours(args, rank, world, local):
     import torch
     import selective_state_space_136_b300 as ss
@@ -661,66 +780,19 @@ def run_ours(args, rank, world, local):
         return
 
     # ---- roofline of the (single) scan kernel
-    hbm_peak, hbm_src = measured_peaks()
-    nbytes = step_bytes(cfg)
-    gbs = nbytes / avg_launch_s / 1e9
-    bdln = elements * cfg.dstate
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    terms = {"hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "peak_source": hbm_src,
-                     "floor_us": nbytes / (hbm_peak * 1e9) * 1e6,
-                     "frac_of_nominal_8000": gbs / 8000.0}}
-    fp32_peak = sms * FP32_LANES_PER_SM * MAX_SM_MHZ * 1e6 / 1e12     # Tops/s
-    fp32_ops = 4.0 * bdln
-    terms["fp32"] = {"achieved": fp32_ops / avg_launch_s / 1e12, "peak": fp32_peak,
-                     "unit": "Tops/s", "floor_us": fp32_ops / (fp32_peak * 1e12) * 1e6,
-                     "note": "4 FMA-pipe lane ops per state element (dt*A, dt*u*B, state FMA, "
-                             "output FMA) against %d lanes/SM at %.0f MHz" % (FP32_LANES_PER_SM,
-                                                                             MAX_SM_MHZ)}
-    if probes and probes["ex2"]["rc"] == 0 and probes["ex2"]["sm_ghz"] > 0:
-        per_clk = probes["ex2"]["ops_per_s"] / (sms * probes["ex2"]["sm_ghz"] * 1e9)
-        per_clk_arch = float(2 ** round(np.log2(max(per_clk, 1e-9))))
-        ex2_peak = sms * per_clk_arch * MAX_SM_MHZ * 1e6 / 1e9            # Gex2/s
-        # all MUFU work of the call: the N decays per element plus softplus (2) and
-        # the gate (2) per (b, d, l)
-        mufu_all = elements * (cfg.dstate + 4)
-        terms["ex2"] = {"achieved": bdln / avg_launch_s / 1e9, "peak": ex2_peak,
-                        "unit": "Gex2/s", "floor_us": bdln / (ex2_peak * 1e9) * 1e6,
-                        "ex2_per_clk_per_sm_measured": per_clk,
-                        "ex2_per_clk_per_sm_used": per_clk_arch,
-                        "mufu_all_ops": mufu_all,
-                        "mufu_all_floor_us": mufu_all / (ex2_peak * 1e9) * 1e6}
-    for t in terms.values():
-        t["frac"] = t["achieved"] / t["peak"]
-    dominant = max(terms, key=lambda k: terms[k]["floor_us"])
-    # informative: the 4 FP32 lane-ops and the ex2 of a state element all take
-    # issue slots of the same warp scheduler (1 warp-instruction per clock per
-    # scheduler, 4 schedulers per SM), so 5 slots per 32 elements bound the
-    # arithmetic before any overhead; not part of the max above
-    issue_floor_us = bdln * 5 / 32 / (4 * sms) / (MAX_SM_MHZ * 1e6) * 1e6
-    issue_term = {"floor_us": issue_floor_us, "frac": issue_floor_us / (avg_launch_s * 1e6),
-                  "note": "5 issue slots (4 FP32 + 1 MUFU) per 32 state elements, 4 schedulers/SM"}
-    # informative: the mixed probe runs ex2 and FFMA2 at the scan's ratio (one
-    # ex2 per four FMA lane-ops) on independent chains; its rate, scaled to the
-    # maximum clock, is what the two units deliver together
-    mixed_term = None
-    if probes and probes.get("mixed", {}).get("rc") == 0 and probes["mixed"]["sm_ghz"] > 0:
-        rate = probes["mixed"]["ops_per_s"] * (MAX_SM_MHZ * 1e-3) / probes["mixed"]["sm_ghz"]
-        per_clk = probes["mixed"]["ops_per_s"] / (sms * probes["mixed"]["sm_ghz"] * 1e9)
-        mixed_term = {"floor_us": bdln / rate * 1e6, "frac": bdln / rate / avg_launch_s,
-                      "elements_per_clk_per_sm": per_clk,
-                      "note": "state elements (1 ex2 + 4 FMA lane-ops) per second that the "
-                              "mixed probe sustains, at the maximum clock"}
-    dt = terms[dominant]
-    roofline = {"bound": "hbm" if dominant == "hbm" else "alu", "term": dominant,
-                "achieved": dt["achieved"], "peak": dt["peak"], "unit": dt["unit"],
-                "frac": dt["frac"], "traffic": committed_traffic(args.config),
-                "algorithmic_bytes_per_launch": nbytes,
-                "kernel_us": avg_launch_s * 1e6,
-                "kernel_note": "time of one ss_scan_fwd call (B/C pack + scan kernels) from CUDA "
-                               "events on the launching stream, averaged over the timed steps",
-                "floor_us": max(t["floor_us"] for t in terms.values()),
-                "frac_of_floor": max(t["floor_us"] for t in terms.values()) / (avg_launch_s * 1e6),
-                "terms": terms, "issue_slots": issue_term, "mixed_units": mixed_term, "peak_clock_mhz": MAX_SM_MHZ}
+    roofline = scan_roofline(cfg, avg_launch_s, probes, sms_of(dev))
+    roofline["traffic"] = committed_traffic(args.config)
+    roofline["kernel_note"] = ("time of one ss_scan_fwd call (B/C pack + scan kernels) from CUDA "
+                               "events on the launching stream, averaged over the timed steps")
+    nbytes = roofline["algorithmic_bytes_per_launch"]
+    gbs = roofline["terms"]["hbm"]["achieved"]
+
+    per_config = None
+    if not args.skip_configs:
+        per_config = {}
+        for name in ("mamba130m", "long1m"):
+            if name != args.config:
+                per_config[name] = time_scan_config(ss, ctx, dev, stream, name, probes)
 
     cpu = None
     if not args.skip_cpu:
@@ -738,9 +810,9 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded normal draws; A=-(n+1); dt bias log-uniform [1e-3,1e-1])",
         "config": dict(workload_config(cfg),
-                       variant=names.get(variant, str(variant)),
-                       l2="no flush: %.0f MB of inputs+outputs per step > 126 MB L2" % (nbytes / 1e6),
                        parallelism="replicas" if world > 1 else "single"),
+        "variant": names.get(variant, str(variant)),
+        "l2": "no flush: %.0f MB of inputs+outputs per step > 126 MB L2" % (nbytes / 1e6),
         "gbs": gbs,
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -753,6 +825,7 @@ def run_ours(args, rank, world, local):
         "conv1d": conv1d,
         "backward": bwd,
         "ssd": ssd,
+        "configs": per_config,
         "impl": "ours",
     }
     print(json.dumps(out), flush=True)
@@ -784,7 +857,8 @@ def run_reference(args, rank, world):
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": cfg.elements / value * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": dict(workload_config(cfg), parallelism="single"),
+           "config": dict(workload_config(cfg),
+                          parallelism="replicas" if world > 1 else "single"),
            "impl": "reference",
            "cpu_baseline": {"value": value, "unit": "elements/s", "cores": cores,
                             "kind": "oracle", "sample": sample},
