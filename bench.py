@@ -377,6 +377,72 @@ def time_conv1d(ss, ctx, dev, stream, cfg, args):
             "steps": steps, "gpu_launches": steps}
 
 
+def time_conv_scan(ss, ctx, dev, stream, cfg, d, params, args, probes):
+    """The width-4 causal convolution fused in front of the scan (x in, y out)
+    against the same two steps as separate calls (conv1d writing u in the input
+    dtype, then the scan reading it), on the benchmark workload's tensors."""
+    import torch
+    g = torch.Generator(device="cpu").manual_seed(12)
+    W = 4
+    w = (torch.randn(cfg.dim, W, generator=g) * 0.5).to(dev)
+    b = (torch.randn(cfg.dim, generator=g) * 0.1).to(dev)
+    shp = (cfg.batch, cfg.dim, cfg.seqlen)
+    y = torch.empty(shp, dtype=torch.float32, device=dev)
+    hl = torch.empty((cfg.batch, cfg.dim, cfg.dstate), dtype=torch.float32, device=dev)
+    cs = torch.empty((cfg.batch, cfg.dim, W - 1), dtype=torch.float32, device=dev)
+    fused = ss.PreparedConvScan(d["u"], w, d["delta"], params["A"], d["B"], d["C"], ctx=ctx,
+                                stream=stream, conv_bias=b, D=params["D"],
+                                delta_bias=params["delta_bias"], z=d["z"], y=y, h_last=hl,
+                                conv_state_out=cs)
+    u = torch.empty_like(d["u"])
+    scan = ss.PreparedScan(u, d["delta"], params["A"], d["B"], d["C"], D=params["D"],
+                           delta_bias=params["delta_bias"], z=d["z"], y=y, h_last=hl, ctx=ctx,
+                           stream=stream)
+
+    def separate():
+        ss.ss_conv1d_fwd(d["u"], w, bias=b, silu=True, out=u, final_state=cs, ctx=ctx,
+                         stream=stream)
+        scan()
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n * 1e-3
+
+    n = max(5, min(args.steps, 20))
+    t_f = timed(fused, n)
+    variant, launches = ctx.last_launch()
+    t_s = timed(separate, n)
+    if ctx.device_error() != ss.SS_OK:
+        raise RuntimeError("device error in the conv+scan leg")
+    esz = 2 if cfg.in_dtype == "bf16" else 4
+    scan_bytes = step_bytes(cfg)
+    conv_state_bytes = cfg.batch * cfg.dim * (W - 1) * 4
+    fused_bytes = scan_bytes + conv_state_bytes + cfg.dim * (W + 1) * 4
+    u_round_trip = 2 * cfg.elements * esz
+    rf = scan_roofline(cfg, t_f, probes, sms_of(dev))
+    return {"workload": "conv1d (width 4, bias, silu) fused in front of the scan: " +
+                        workload_config(cfg)["workload"],
+            "us_fused": t_f * 1e6, "us_separate": t_s * 1e6,
+            "elements_per_s_fused": cfg.elements / t_f,
+            "algorithmic_bytes_fused": fused_bytes,
+            "algorithmic_bytes_separate": fused_bytes + u_round_trip,
+            "bytes_saved": u_round_trip,
+            "roofline_scan_terms": {"bound": rf["bound"], "term": rf["term"],
+                                    "frac_of_floor": rf["frac_of_floor"],
+                                    "floor_us": rf["floor_us"],
+                                    "note": "the scan's own floor (the convolution adds 4 FMAs "
+                                            "and a silu per (b, d, l))"},
+            "launches_fused": launches, "steps": n, "gpu_launches": n * (launches + 3)}
+
+
 def time_bwd(ss, ctx, dev, stream, cfg, d, params, args):
     """Time ss_scan_bwd on the scan workload (the forward inputs already on the
     device, dy fp32, all gradients requested)."""
@@ -707,6 +773,8 @@ def run_ours(args, rank, world, local):
     decode = None if args.skip_decode else time_decode(ss, ctx, dev, stream, args)
     conv1d = None if args.skip_conv else time_conv1d(ss, ctx, dev, stream, cfg, args)
     bwd = None if args.skip_bwd else time_bwd(ss, ctx, dev, stream, cfg, d, params, args)
+    conv_scan = None if args.skip_conv else time_conv_scan(ss, ctx, dev, stream, cfg, d, params,
+                                                           args, probes)
     ssd = None if args.skip_ssd else time_ssd(ss, ctx, dev, stream, args, probes=probes)
 
     # ---- end to end: pinned host inputs in, y and h_last back to host, every step.
@@ -823,6 +891,7 @@ def run_ours(args, rank, world, local):
         "alu_probe": probes,
         "decode": decode,
         "conv1d": conv1d,
+        "conv_scan": conv_scan,
         "backward": bwd,
         "ssd": ssd,
         "configs": per_config,

@@ -246,6 +246,49 @@ typedef struct {
 int ss_conv1d_fwd(ss_ctx *ctx, const ss_conv1d_args *args, ss_stream_t stream);
 
 /*
+ * The Mamba block's convolution fused in front of the selective scan: the
+ * convolution of ss_conv1d_fwd (its silu applied when conv_silu != 0) gives
+ * u, and the scan of ss_scan_fwd runs on that u, in one pass over the inputs
+ * ("Mamba: Linear-Time Sequence Modeling with Selective State Spaces",
+ * section "Key terms": the block's 1D convolution feeds the selective SSM;
+ * same page, section "Hardware-aware state expansion": inputs cross into
+ * on-chip memory once). Per row (b, d), W = conv_width:
+ *     c[l] = conv_bias[d] + sum_{k<W} conv_weight[d,k] * xin(l-(W-1)+k)
+ *     xin(j) = x[b,d,j] for j >= 0; conv_init[b,d,(W-1)+j] for j < 0
+ *              (zero when conv_init is NULL)
+ *     u[l] = silu(c[l]) when conv_silu != 0, else c[l]
+ *     y, h_last: ss_scan_fwd on (u, delta, z, A, B, C, D, delta_bias, h0)
+ *   scan           : as for ss_scan_fwd, except that scan.u holds x, the
+ *                    convolution's input (batch, dim, seqlen) in in_dtype.
+ *                    u is kept in fp32 (never rounded to in_dtype) inside.
+ *   conv_width     : 2, 3 or 4 (else SS_ERR_UNSUPPORTED).
+ *   conv_weight    : (dim, conv_width) fp32.   conv_bias: (dim) fp32 or NULL.
+ *   conv_init      : (batch, dim, conv_width-1) fp32, oldest input first, or NULL.
+ *   u_out          : (batch, dim, seqlen) in in_dtype, 32-byte aligned, or
+ *                    NULL: receives u rounded to in_dtype (for a backward).
+ *   conv_state_out : (batch, dim, conv_width-1) fp32 or NULL: the last
+ *                    conv_width-1 inputs, the convolution's decode state.
+ * Outputs must not overlap inputs or each other (h_last == h0 is allowed).
+ * Only the chained pair-row kernel carries the fusion: dstate 16, seqlen a
+ * multiple of 16, u, delta, z, y 32-byte aligned, the simplified input
+ * matrix, and variant AUTO, CHUNKED or ROWS with 0 or 2 threads per row;
+ * anything else returns SS_ERR_UNSUPPORTED (compose ss_conv1d_fwd and
+ * ss_scan_fwd there). seqlen == 0 writes h_last = h0 (or zeros) and
+ * conv_state_out = conv_init (or zeros).
+ */
+typedef struct {
+    ss_scan_args scan;
+    int conv_width;
+    const float *conv_weight, *conv_bias;
+    const float *conv_init;
+    int conv_silu;
+    void *u_out;
+    float *conv_state_out;
+} ss_conv_scan_args;
+
+int ss_conv_scan_fwd(ss_ctx *ctx, const ss_conv_scan_args *args, ss_stream_t stream);
+
+/*
  * One decode step of the convolution, per row (b, d):
  *     out = bias[d] + sum_{k<W-1} weight[d,k] * state[b,d,k] + weight[d,W-1] * x[b,d]
  *     (then silu when silu != 0); state drops its oldest input and appends x.

@@ -204,6 +204,33 @@ def conv1d_fwd(x, weight, bias=None, init_state=None, silu=False, rows=None, dim
     return out.reshape(out_shape), fs[:, :W - 1].reshape(st_shape)
 
 
+def conv_scan_fwd(x, conv_weight, delta, A, B, C, conv_bias=None, conv_init=None, conv_silu=True,
+                  D=None, delta_bias=None, z=None, delta_softplus=True, h0=None, rows=None,
+                  dim=None):
+    """The Mamba block's convolution followed by the selective scan, in that
+    order ("Mamba: Linear-Time Sequence Modeling with Selective State Spaces",
+    section "Key terms": the block's 1D convolution feeds the SSM): u =
+    conv1d_fwd(x, ...) (silu applied when conv_silu), then scan_fwd on u.
+
+    The convolution's fp64 output is handed to the scan as float32 (the scan
+    reads float32 or bf16 inputs); delta, z, B and C are widened to float32,
+    which is exact for bf16. Same full-tensor or row-subset forms as scan_fwd.
+    Returns (y, h_last, u, conv_final_state), u and the state in float64."""
+    u, fs = conv1d_fwd(x, conv_weight, bias=conv_bias, init_state=conv_init, silu=conv_silu,
+                       rows=rows, dim=dim)
+    wide = lambda a: None if a is None else (
+        _bf16_to_f32(a) if np.asarray(a).dtype == np.uint16 else np.asarray(a, dtype=np.float32))
+    y, h = scan_fwd(u.astype(np.float32), wide(delta), A, wide(B), wide(C), D=D,
+                    delta_bias=delta_bias, z=wide(z), delta_softplus=delta_softplus, h0=h0,
+                    rows=rows, dim=dim)
+    return y, h, u, fs
+
+
+def _bf16_to_f32(a):
+    a = np.ascontiguousarray(a)
+    return (a.astype(np.uint32) << 16).view(np.float32)
+
+
 def conv1d_update(state, x, weight, bias=None, silu=False, dim=None):
     """One decode step of the convolution in fp64. state (batch, dim, W-1)
     float64 (oldest input first) is updated in place; x is (batch, dim).

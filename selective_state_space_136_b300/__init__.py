@@ -38,6 +38,13 @@ class ScanArgs(ctypes.Structure):
                 ("delta_softplus", ctypes.c_int), ("h0", _vp), ("y", _vp), ("h_last", _vp)]
 
 
+class ConvScanArgs(ctypes.Structure):
+    """Mirror of ss_conv_scan_args."""
+    _fields_ = [("scan", ScanArgs), ("conv_width", ctypes.c_int), ("conv_weight", _vp),
+                ("conv_bias", _vp), ("conv_init", _vp), ("conv_silu", ctypes.c_int),
+                ("u_out", _vp), ("conv_state_out", _vp)]
+
+
 class UpdateArgs(ctypes.Structure):
     """Mirror of ss_update_args."""
     _fields_ = [("batch", ctypes.c_int), ("dim", ctypes.c_int), ("dstate", ctypes.c_int),
@@ -104,6 +111,7 @@ def lib():
             L.ss_create.argtypes = [ctypes.POINTER(_vp), ctypes.c_int]
             L.ss_destroy.argtypes = [_vp]
             L.ss_scan_fwd.argtypes = [_vp, ctypes.POINTER(ScanArgs), _vp]
+            L.ss_conv_scan_fwd.argtypes = [_vp, ctypes.POINTER(ConvScanArgs), _vp]
             L.ss_state_update.argtypes = [_vp, ctypes.POINTER(UpdateArgs), _vp]
             L.ss_conv1d_fwd.argtypes = [_vp, ctypes.POINTER(Conv1dArgs), _vp]
             L.ss_scan_bwd.argtypes = [_vp, ctypes.POINTER(ScanBwdArgs), _vp]
@@ -115,7 +123,7 @@ def lib():
             L.ss_set_option.argtypes = [_vp, ctypes.c_int, ctypes.c_longlong]
             L.ss_last_launch.argtypes = [_vp, ctypes.POINTER(ctypes.c_int),
                                          ctypes.POINTER(ctypes.c_int)]
-            for f in ("ss_create", "ss_destroy", "ss_scan_fwd", "ss_state_update",
+            for f in ("ss_create", "ss_destroy", "ss_scan_fwd", "ss_conv_scan_fwd", "ss_state_update",
                       "ss_get_device_error", "ss_set_option", "ss_last_launch"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
@@ -303,6 +311,106 @@ class PreparedScan:
         if rc != SS_OK:
             raise SSError(rc, "ss_scan_fwd")
         return self.y, self.h_last
+
+
+def _conv_scan_args(x, conv_weight, delta, A, B, C, conv_bias, conv_init, conv_silu, D,
+                    delta_bias, z, delta_softplus, h0, y, h_last, out_dtype, u_out,
+                    conv_state_out, want_u, want_conv_state):
+    """Checks and marshals the arguments of ss_conv_scan_fwd; allocates the
+    outputs that were asked for but not given."""
+    import torch
+    _need(x, "x")
+    batch, dim, L = x.shape
+    N = B.shape[1]
+    dev = x.device
+    _need(conv_weight, "conv_weight", None, torch.float32, dev)
+    if conv_weight.dim() != 2 or conv_weight.shape[0] != dim:
+        raise ValueError("conv_weight must be (dim, width)")
+    W = conv_weight.shape[1]
+    _need(delta, "delta", x.shape, x.dtype, dev)
+    if z is not None:
+        _need(z, "z", x.shape, x.dtype, dev)
+    _need(B, "B", (batch, N, L), x.dtype, dev)
+    _need(C, "C", (batch, N, L), x.dtype, dev)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    for t, name in ((D, "D"), (delta_bias, "delta_bias"), (conv_bias, "conv_bias")):
+        if t is not None:
+            _need(t, name, (dim,), torch.float32, dev)
+    if conv_init is not None:
+        _need(conv_init, "conv_init", (batch, dim, W - 1), torch.float32, dev)
+    if h0 is not None:
+        _need(h0, "h0", (batch, dim, N), torch.float32, dev)
+    if y is None:
+        y = torch.empty((batch, dim, L), dtype=out_dtype or torch.float32, device=dev)
+    _need(y, "y", (batch, dim, L), None, dev)
+    if h_last is None:
+        h_last = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    _need(h_last, "h_last", (batch, dim, N), torch.float32, dev)
+    if u_out is None and want_u:
+        u_out = torch.empty((batch, dim, L), dtype=x.dtype, device=dev)
+    if u_out is not None:
+        _need(u_out, "u_out", x.shape, x.dtype, dev)
+    if conv_state_out is None and want_conv_state:
+        conv_state_out = torch.empty((batch, dim, W - 1), dtype=torch.float32, device=dev)
+    if conv_state_out is not None:
+        _need(conv_state_out, "conv_state_out", (batch, dim, W - 1), torch.float32, dev)
+    scan = ScanArgs(batch, dim, N, L, _dtype_code(x), _dtype_code(y), _p(x), _p(delta), _p(z),
+                    _p(A), _p(B), _p(C), _p(D), _p(delta_bias), int(bool(delta_softplus)),
+                    _p(h0), _p(y), _p(h_last))
+    a = ConvScanArgs(scan, W, _p(conv_weight), _p(conv_bias), _p(conv_init), int(bool(conv_silu)),
+                     _p(u_out), _p(conv_state_out))
+    keep = (x, conv_weight, delta, A, B, C, conv_bias, conv_init, D, delta_bias, z, h0)
+    return a, dev, (y, h_last, u_out, conv_state_out), keep
+
+
+def ss_conv_scan_fwd(x, conv_weight, delta, A, B, C, conv_bias=None, conv_init=None,
+                     conv_silu=True, D=None, delta_bias=None, z=None, delta_softplus=True,
+                     h0=None, y=None, h_last=None, out_dtype=None, u_out=None,
+                     conv_state_out=None, return_u=False, return_conv_state=False,
+                     ctx: Context | None = None, stream=None):
+    """The Mamba block's causal conv1d fused in front of the selective scan.
+
+    x (the convolution's input), delta, z: (batch, dim, L); B, C: (batch, N, L);
+    conv_weight (dim, width) float32, width 2..4; conv_bias (dim,) and
+    conv_init (batch, dim, width-1) float32 or None. u = silu(conv(x)) (conv(x)
+    when conv_silu is False) feeds the scan as in ss_scan_fwd. Returns
+    (y, h_last, u_out, conv_state_out): the last two are None unless given or
+    asked for with return_u / return_conv_state. Asynchronous."""
+    a, dev, outs, _ = _conv_scan_args(x, conv_weight, delta, A, B, C, conv_bias, conv_init,
+                                      conv_silu, D, delta_bias, z, delta_softplus, h0, y, h_last,
+                                      out_dtype, u_out, conv_state_out, return_u,
+                                      return_conv_state)
+    ctx = ctx or default_context(dev.index if dev.index is not None else 0)
+    _check(lib().ss_conv_scan_fwd(ctx.handle, ctypes.byref(a), _stream_ptr(stream, dev)),
+           "ss_conv_scan_fwd")
+    return outs
+
+
+class PreparedConvScan:
+    """An ss_conv_scan_fwd call whose arguments were checked and marshalled
+    once (see PreparedScan); outputs are held in .outputs."""
+
+    def __init__(self, x, conv_weight, delta, A, B, C, ctx: Context | None = None, stream=None,
+                 **kw):
+        args = dict(conv_bias=None, conv_init=None, conv_silu=True, D=None, delta_bias=None,
+                    z=None, delta_softplus=True, h0=None, y=None, h_last=None, out_dtype=None,
+                    u_out=None, conv_state_out=None, return_u=False, return_conv_state=False)
+        args.update(kw)
+        self._args, dev, self.outputs, self._keep = _conv_scan_args(
+            x, conv_weight, delta, A, B, C, args["conv_bias"], args["conv_init"],
+            args["conv_silu"], args["D"], args["delta_bias"], args["z"], args["delta_softplus"],
+            args["h0"], args["y"], args["h_last"], args["out_dtype"], args["u_out"],
+            args["conv_state_out"], args["return_u"], args["return_conv_state"])
+        self.ctx = ctx or default_context(dev.index if dev.index is not None else 0)
+        self._stream = _stream_ptr(stream, dev)
+        self._fn = lib().ss_conv_scan_fwd
+        self._argp = ctypes.byref(self._args)
+
+    def __call__(self):
+        rc = self._fn(self.ctx.handle, self._argp, self._stream)
+        if rc != SS_OK:
+            raise SSError(rc, "ss_conv_scan_fwd")
+        return self.outputs
 
 
 def ss_state_update(state, x, dt, A, B, C, D=None, dt_bias=None, z=None, dt_softplus=True,

@@ -54,6 +54,8 @@ int ensure_pair_scratch(ss_ctx *ctx, const ssh::ScanParams &p, int n_seg, bool c
     return SS_OK;
 }
 
+int dispatch_scan(ss_ctx *ctx, const ssh::ScanParams &p, cudaStream_t st);
+
 int set_device(const ss_ctx *ctx) {
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) return SS_ERR_CUDA;
@@ -239,28 +241,30 @@ int ss_scan_fwd(ss_ctx *ctx, const ss_scan_args *a, ss_stream_t stream) {
                       a->u, a->delta, a->z, a->A, a->B, a->C, a->D, a->delta_bias,
                       a->delta_softplus, a->h0, a->y, a->h_last, ctx->d_err, ctx->wait_limit,
                       ctx->drop_tile, ctx->zoh};
-    int variant = ctx->variant;
-    const bool rows_ok = ssh::rows_supported(p) && ssh::seq_supported(p);
-    // the exact zero-order hold runs on the one-thread-per-row kernels only
-    const bool pair_ok = ssh::pair_supported(p) && !ctx->zoh;
-    const long long resident = (long long)(ctx->warps_per_sm > 0 ? ctx->warps_per_sm : 8) *
-                               ctx->sm_count;
-    if (variant == SS_VARIANT_AUTO) {
-        // few row blocks for the machine: scan time segments in parallel
-        if (pair_ok && 2LL * ssh::pair_row_blocks(p) < resident) variant = SS_VARIANT_CHUNKED;
-        else variant = rows_ok ? SS_VARIANT_ROWS : SS_VARIANT_SIMPLE;
-    }
-    if (variant == SS_VARIANT_ROWS && !rows_ok) return SS_ERR_UNSUPPORTED;
-    int rc, launches = 1;
-    if (variant == SS_VARIANT_CHUNKED) {
-        if (!pair_ok) return SS_ERR_UNSUPPORTED;
+    return dispatch_scan(ctx, p, st);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Launch the chained pair-row kernel (one pass) or its chunked variant (time
+// segments scanned in parallel, then combined) for p; the rule is the one
+// SS_VARIANT_AUTO uses: chunked when there are fewer than half as many row
+// blocks as resident warps.
+int run_pair(ss_ctx *ctx, const ssh::ScanParams &p, bool chunked, cudaStream_t st,
+             int *launches) {
+    int rc;
+    if (chunked) {
+        const long long resident = (long long)(ctx->warps_per_sm > 0 ? ctx->warps_per_sm : 8) *
+                                   ctx->sm_count;
         int req = ctx->segments;
         if (req <= 0) {
             // at least one unit per resident warp, and segments of at most 8192
             // steps so long sequences split into many small balanced units
             const long long rb = ssh::pair_row_blocks(p);
             long long r = (resident + rb - 1) / rb;
-            const long long by_len = (a->seqlen + 8191) / 8192;
+            const long long by_len = (p.seqlen + 8191) / 8192;
             if (by_len > r) r = by_len;
             req = (int)(r < 2 ? 2 : (r > 65535 ? 65535 : r));
         }
@@ -271,23 +275,48 @@ int ss_scan_fwd(ss_ctx *ctx, const ss_scan_args *a, ss_stream_t stream) {
         w.sm_count = ctx->sm_count;
         w.warps_per_sm = ctx->warps_per_sm;
         w.n_seg = n_seg;
-        rc = ssh::launch_pair(p, w, st);
-        launches = n_seg >= 2 ? 4 : 2;
+        *launches = n_seg >= 2 ? 4 : 2;
+        return ssh::launch_pair(p, w, st);
+    }
+    ssh::PairWork w{};
+    const int n_seg = 1;  // the chained kernel balances by tile ranges, not segments
+    if ((rc = ensure_pair_scratch(ctx, p, n_seg, false, &w)) != SS_OK) return rc;
+    w.epoch = ++ctx->epoch;
+    w.sm_count = ctx->sm_count;
+    w.warps_per_sm = ctx->warps_per_sm;
+    w.n_seg = n_seg;
+    *launches = 2;
+    return ssh::launch_pair(p, w, st);
+}
+
+bool prefer_chunked(const ss_ctx *ctx, const ssh::ScanParams &p) {
+    const long long resident = (long long)(ctx->warps_per_sm > 0 ? ctx->warps_per_sm : 8) *
+                               ctx->sm_count;
+    return 2LL * ssh::pair_row_blocks(p) < resident;
+}
+
+int dispatch_scan(ss_ctx *ctx, const ssh::ScanParams &p, cudaStream_t st) {
+    int variant = ctx->variant;
+    const bool rows_ok = ssh::rows_supported(p) && ssh::seq_supported(p);
+    // the exact zero-order hold runs on the one-thread-per-row kernels only
+    const bool pair_ok = ssh::pair_supported(p) && !ctx->zoh;
+    if (variant == SS_VARIANT_AUTO) {
+        // few row blocks for the machine: scan time segments in parallel
+        if (pair_ok && prefer_chunked(ctx, p)) variant = SS_VARIANT_CHUNKED;
+        else variant = rows_ok ? SS_VARIANT_ROWS : SS_VARIANT_SIMPLE;
+    }
+    if (variant == SS_VARIANT_ROWS && !rows_ok) return SS_ERR_UNSUPPORTED;
+    int rc, launches = 1;
+    if (variant == SS_VARIANT_CHUNKED) {
+        if (!pair_ok) return SS_ERR_UNSUPPORTED;
+        rc = run_pair(ctx, p, true, st, &launches);
     } else if (variant == SS_VARIANT_ROWS) {
         int tpr = ctx->rows_tpr;
         if (tpr == 0) tpr = pair_ok ? 2 : 1;
         if (ctx->zoh && tpr != 1) return SS_ERR_UNSUPPORTED;
         if (tpr == 2) {
             if (!pair_ok) return SS_ERR_UNSUPPORTED;
-            ssh::PairWork w{};
-            const int n_seg = 1;  // the chained kernel balances by tile ranges, not segments
-            if ((rc = ensure_pair_scratch(ctx, p, n_seg, false, &w)) != SS_OK) return rc;
-            w.epoch = ++ctx->epoch;
-            w.sm_count = ctx->sm_count;
-            w.warps_per_sm = ctx->warps_per_sm;
-            w.n_seg = n_seg;
-            rc = ssh::launch_pair(p, w, st);
-            launches = 2;
+            rc = run_pair(ctx, p, false, st, &launches);
         } else if (tpr == 1) {
             rc = ssh::launch_seq(p, ctx->max_smem_optin, st);
         } else {
@@ -297,6 +326,98 @@ int ss_scan_fwd(ss_ctx *ctx, const ss_scan_args *a, ss_stream_t stream) {
         rc = ssh::launch_simple(p, st);
     }
     ctx->last_variant = variant;
+    ctx->last_launches = rc == SS_OK ? launches : 0;
+    return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ss_conv_scan_fwd(ss_ctx *ctx, const ss_conv_scan_args *ca, ss_stream_t stream) {
+    if (!ctx || !ca) return SS_ERR_INVALID_ARG;
+    const ss_scan_args *a = &ca->scan;
+    if (a->batch < 1 || a->dim < 1 || a->seqlen < 0) return SS_ERR_INVALID_ARG;
+    if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return SS_ERR_INVALID_ARG;
+    if (ca->conv_width < 2 || ca->conv_width > 4) return SS_ERR_UNSUPPORTED;
+    if (a->dstate != 16) return SS_ERR_UNSUPPORTED;
+    if ((long long)a->batch * a->dim > (1LL << 40) || a->seqlen >= (1LL << 40))
+        return SS_ERR_INVALID_ARG;
+    if (!a->A || !ca->conv_weight) return SS_ERR_INVALID_ARG;
+    if (a->seqlen > 0 && (!a->u || !a->delta || !a->B || !a->C || !a->y))
+        return SS_ERR_INVALID_ARG;
+    const void *ptrs[] = {a->u, a->delta, a->z, a->A, a->B, a->C, a->D, a->delta_bias, a->h0,
+                          a->y, a->h_last, ca->conv_weight, ca->conv_bias, ca->conv_init,
+                          ca->u_out, ca->conv_state_out};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return SS_ERR_INVALID_ARG;
+    const long long rows = (long long)a->batch * a->dim;
+    const size_t esz = a->in_dtype == SS_BF16 ? 2 : 4, osz = a->out_dtype == SS_BF16 ? 2 : 4;
+    const size_t n_elem = (size_t)rows * (size_t)a->seqlen;
+    const size_t n_bc = (size_t)a->batch * 16 * (size_t)a->seqlen;
+    const size_t n_state = (size_t)rows * 16;
+    const size_t n_cst = (size_t)rows * (size_t)(ca->conv_width - 1);
+    // every output against every input and against the other outputs
+    const Span ins[] = {span(a->u, n_elem * esz), span(a->delta, n_elem * esz),
+                        span(a->z, a->z ? n_elem * esz : 0), span(a->B, n_bc * esz),
+                        span(a->C, n_bc * esz), span(a->A, (size_t)a->dim * 16 * 4),
+                        span(a->D, a->D ? (size_t)a->dim * 4 : 0),
+                        span(a->delta_bias, a->delta_bias ? (size_t)a->dim * 4 : 0),
+                        span(a->h0, a->h0 ? n_state * 4 : 0),
+                        span(ca->conv_weight, (size_t)a->dim * ca->conv_width * 4),
+                        span(ca->conv_bias, ca->conv_bias ? (size_t)a->dim * 4 : 0),
+                        span(ca->conv_init, ca->conv_init ? n_cst * 4 : 0)};
+    const Span outs[] = {span(a->y, a->seqlen > 0 ? n_elem * osz : 0),
+                         span(a->h_last, a->h_last ? n_state * 4 : 0),
+                         span(ca->u_out, ca->u_out ? n_elem * esz : 0),
+                         span(ca->conv_state_out, ca->conv_state_out ? n_cst * 4 : 0)};
+    const size_t n_out = sizeof(outs) / sizeof(outs[0]);
+    for (size_t i = 0; i < n_out; ++i) {
+        for (const Span &in : ins) {
+            // h_last may be h0 itself (read, then written per row)
+            if (i == 1 && a->h0 && a->h_last == a->h0 && in.lo == span(a->h0, 1).lo) continue;
+            if (overlaps(outs[i], in)) return SS_ERR_INVALID_ARG;
+        }
+        for (size_t j = i + 1; j < n_out; ++j)
+            if (overlaps(outs[i], outs[j])) return SS_ERR_INVALID_ARG;
+    }
+    if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    ctx->last_launches = 0;
+    ctx->last_variant = SS_VARIANT_AUTO;
+    if (a->seqlen == 0) {
+        if (a->h_last) {
+            const cudaError_t e = a->h0 ? (a->h0 == a->h_last ? cudaSuccess
+                                                              : cudaMemcpyAsync(a->h_last, a->h0, n_state * 4,
+                                                                                cudaMemcpyDeviceToDevice, st))
+                                        : cudaMemsetAsync(a->h_last, 0, n_state * 4, st);
+            if (e != cudaSuccess) return SS_ERR_CUDA;
+        }
+        if (ca->conv_state_out) {
+            const cudaError_t e = ca->conv_init
+                                      ? cudaMemcpyAsync(ca->conv_state_out, ca->conv_init, n_cst * 4,
+                                                        cudaMemcpyDeviceToDevice, st)
+                                      : cudaMemsetAsync(ca->conv_state_out, 0, n_cst * 4, st);
+            if (e != cudaSuccess) return SS_ERR_CUDA;
+        }
+        return SS_OK;
+    }
+    ssh::ScanParams p{a->batch, a->dim, a->dstate, a->seqlen, a->in_dtype, a->out_dtype,
+                      a->u, a->delta, a->z, a->A, a->B, a->C, a->D, a->delta_bias,
+                      a->delta_softplus, a->h0, a->y, a->h_last, ctx->d_err, ctx->wait_limit,
+                      ctx->drop_tile, ctx->zoh, ca->conv_width, ca->conv_silu, ca->conv_weight,
+                      ca->conv_bias, ca->conv_init, ca->conv_state_out, ca->u_out};
+    // the fused convolution lives in the chained pair-row kernel only (its u_out
+    // stores whole 32-byte sectors, like y)
+    if (!ssh::pair_supported(p) || ctx->zoh) return SS_ERR_UNSUPPORTED;
+    if (ca->u_out && (reinterpret_cast<uintptr_t>(ca->u_out) & 31u) != 0) return SS_ERR_UNSUPPORTED;
+    bool chunked = prefer_chunked(ctx, p);
+    if (ctx->variant == SS_VARIANT_CHUNKED) chunked = true;
+    else if (ctx->variant == SS_VARIANT_ROWS && (ctx->rows_tpr == 0 || ctx->rows_tpr == 2)) chunked = false;
+    else if (ctx->variant != SS_VARIANT_AUTO) return SS_ERR_UNSUPPORTED;
+    int launches = 0;
+    const int rc = run_pair(ctx, p, chunked, st, &launches);
+    ctx->last_variant = chunked ? SS_VARIANT_CHUNKED : SS_VARIANT_ROWS;
     ctx->last_launches = rc == SS_OK ? launches : 0;
     return rc;
 }

@@ -188,6 +188,17 @@ __device__ __forceinline__ f2 silu2_tanh(f2 z) {
     const f2 hz = fmul2(z, mk2(0.5f, 0.5f));
     return ffma2(hz, mk2(tanh_approx(hz.x), tanh_approx(hz.y)), hz);
 }
+// The factor g of silu(x) = x * g(x), i.e. sigmoid(x): (1 + tanh(x/2)) / 2 on
+// the tanh unit (bf16-input path), 1 / (1 + 2^(-x log2 e)) otherwise.
+__device__ __forceinline__ f2 silu2_gate_tanh(f2 x) {
+    const f2 hx = fmul2(x, mk2(0.5f, 0.5f));
+    return ffma2(mk2(0.5f, 0.5f), mk2(tanh_approx(hx.x), tanh_approx(hx.y)), mk2(0.5f, 0.5f));
+}
+__device__ __forceinline__ f2 silu2_gate(f2 x) {
+    const f2 t = fmul2(x, mk2(-kLog2e, -kLog2e));
+    const f2 d = fadd2(mk2(ex2(t.x), ex2(t.y)), mk2(1.f, 1.f));
+    return mk2(rcp_approx(d.x), rcp_approx(d.y));
+}
 __device__ __forceinline__ f2 silu2(f2 z) {
     const f2 t = fmul2(z, mk2(-kLog2e, -kLog2e));
     const f2 d = fadd2(mk2(ex2(t.x), ex2(t.y)), mk2(1.f, 1.f));

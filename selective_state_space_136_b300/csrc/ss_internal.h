@@ -49,6 +49,16 @@ struct ScanParams {
     uint32_t wait_limit;
     int drop_tile;
     int zoh;  // exact zero-order-hold input matrix (one-thread-per-row kernels only)
+    // causal conv1d fused in front of the scan (chained pair-row kernel only):
+    // with conv_width > 0, `u` holds the convolution's input x and the scan's
+    // u is silu(conv(x)) (conv(x) when conv_silu == 0), formed in registers
+    int conv_width;           // 0 (no convolution) or 2..4
+    int conv_silu;
+    const float *conv_w;      // (dim, conv_width)
+    const float *conv_b;      // (dim) or null
+    const float *conv_init;   // (batch, dim, conv_width - 1) or null (zeros)
+    float *conv_state;        // (batch, dim, conv_width - 1) out, or null
+    void *u_out;              // (batch, dim, seqlen) in in_dtype out, or null
 };
 
 int launch_simple(const ScanParams &p, cudaStream_t st);

@@ -62,7 +62,9 @@ struct PairLayout {
     static constexpr int NV = TL * ESZ / 32;           // 32-byte loads per row per tensor per tile
     static constexpr int BC_BOX = TL * 2 * kN * 4;     // fp32 [TL][B16 C16]
     static constexpr int OFF_BAR = S * BC_BOX;
-    static constexpr int TOTAL = OFF_BAR + S * 8 + 128;
+    static constexpr int OFF_CONV = OFF_BAR + 64;       // fused convolution: 32 lanes x 8 floats
+    static constexpr int TOTAL = OFF_CONV + 32 * 8 * 4 + 128;
+    static_assert(S * 8 <= 64, "mbarriers fit before the convolution's slots");
     static_assert(BC_BOX % 128 == 0, "TMA destinations 128-byte aligned");
     static_assert(NV >= 1 && TL * ESZ % 32 == 0, "a tile row is whole 32-byte sectors");
 };
@@ -248,7 +250,7 @@ enum { kChain = 0, kAgg = 1, kSeg = 2 };
 #define SS_PAIR_BOUNDS __launch_bounds__(32, SS_PAIR_MINB)
 #endif
 
-template <typename Tin, typename Tout, int TL, int S, int MODE>
+template <typename Tin, typename Tout, int TL, int S, int MODE, bool CV>
 __global__ void SS_PAIR_BOUNDS
     scan_pair_kernel(const __grid_constant__ CUtensorMap tm_bc, const ssh::ScanParams p,
                      const PairSched sch) {
@@ -387,10 +389,33 @@ __global__ void SS_PAIR_BOUNDS
         }
         const float bias = p.bias ? p.bias[dc] : 0.f;
         const float Dd = p.D ? p.D[dc] : 0.f;
-        const Tin *g_u = static_cast<const Tin *>(p.u) + row * L;
+        const Tin *g_u = static_cast<const Tin *>(p.u) + row * L;  // u, or the conv's x
         const Tin *g_dl = static_cast<const Tin *>(p.delta) + row * L;
         const Tin *g_z = has_z ? static_cast<const Tin *>(p.z) + row * L : g_u;
         float sdt = 0.f, sdt_c = 0.f;  // summed dt of the own row (aggregate pass), compensated
+
+        // fused convolution (own row), kept in this lane's shared-memory slot
+        // between tiles (registers are the scan's): the weights right-aligned in
+        // 4 taps (a narrower filter has leading zero taps), the bias, and the 3
+        // inputs before the next tile (earlier steps of x, else the initial
+        // state, else zero)
+        float *cslot = reinterpret_cast<float *>(smem + LY::OFF_CONV) + 8 * lane;
+        if constexpr (CV) {
+            const int W = p.conv_width;
+            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k < W; ++k) v[4 - W + k] = p.conv_w[(long long)dc * W + k];
+            v[4] = p.conv_b ? p.conv_b[dc] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                const int idx = l_begin - 3 + j;  // step of x
+                const int slot = (W - 1) + idx;   // slot of the initial state when idx < 0
+                v[5 + j] = idx >= 0 ? to_f32(g_u[idx])
+                                    : ((p.conv_init && slot >= 0)
+                                           ? p.conv_init[row * (W - 1) + slot] : 0.f);
+            }
+            reinterpret_cast<float4 *>(cslot)[0] = make_float4(v[0], v[1], v[2], v[3]);
+            reinterpret_cast<float4 *>(cslot)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
 
         // B/C tile k of this unit into ring stage (gt + k) % S
         auto issue_bc = [&](int k) {
@@ -427,13 +452,58 @@ __global__ void SS_PAIR_BOUNDS
             (void)zw;
             // (for fp32 inputs the NV loads of a tensor are consecutive registers)
 
+            // own row: u of the tile; with the fused convolution its output,
+            // otherwise the loaded words, widened where they are used
+            f2 uv[CV ? TL / 2 : 1] = {};
+            auto u_at = [&](int i) -> f2 {
+                if constexpr (CV) return uv[i];
+                else return pair_at(uw, i, Tin());
+            };
+            if constexpr (CV) {
+                // x of the tile and the 3 inputs before it: c[l] = cb + sum_k cw[k] x[l-3+k]
+                const float4 s0 = reinterpret_cast<const float4 *>(cslot)[0];
+                const float4 s1 = reinterpret_cast<const float4 *>(cslot)[1];
+                const float cw[4] = {s0.x, s0.y, s0.z, s0.w}, cb = s1.x;
+                float xv[TL + 3];
+                xv[0] = s1.y, xv[1] = s1.z, xv[2] = s1.w;
+#pragma unroll
+                for (int i = 0; i < TL / 2; ++i) {
+                    const f2 w2 = pair_at(uw, i, Tin());
+                    xv[3 + 2 * i] = w2.x;
+                    xv[3 + 2 * i + 1] = w2.y;
+                }
+#pragma unroll
+                for (int i = 0; i < TL / 2; ++i) {
+                    f2 c2 = mk2(cb, cb);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        c2 = ffma2(mk2(cw[k], cw[k]), mk2(xv[2 * i + k], xv[2 * i + 1 + k]), c2);
+                    uv[i] = !p.conv_silu ? c2
+                                         : ((SS_PAIR_TANH && sizeof(Tin) == 2) ? fmul2(c2, silu2_gate_tanh(c2))
+                                                                             : fmul2(c2, silu2_gate(c2)));
+                }
+                reinterpret_cast<float4 *>(cslot)[1] = make_float4(cb, xv[TL], xv[TL + 1], xv[TL + 2]);
+                if (OUT && p.u_out && row_ok) {
+                    float uo[TL];
+#pragma unroll
+                    for (int i = 0; i < TL / 2; ++i) uo[2 * i] = uv[i].x, uo[2 * i + 1] = uv[i].y;
+                    store_tile<TL>(static_cast<Tin *>(p.u_out) + row * (long long)L + l_begin + k * TL, uo);
+                }
+                if (OUT && p.conv_state && row_ok && k + 1 == n_tiles &&
+                    (MODE == kSeg ? seg + 1 == sch.n_seg : at_end)) {
+                    const int W = p.conv_width;
+                    for (int j = 0; j < W - 1; ++j)
+                        p.conv_state[row * (W - 1) + j] = xv[TL + 3 - (W - 1) + j];
+                }
+            }
+
             // own row: dt and dt*u for the tile (each (row, step) once)
             f2 dt[TL / 2], du[TL / 2];
 #pragma unroll
             for (int i = 0; i < TL / 2; ++i) {
                 const f2 x = fadd2(pair_at(dw, i, Tin()), mk2(bias, bias));
                 dt[i] = p.softplus ? softplus2_d6(x) : x;
-                du[i] = fmul2(dt[i], pair_at(uw, i, Tin()));
+                du[i] = fmul2(dt[i], u_at(i));
             }
             if (MODE == kAgg) {
                 // pairwise sum of the tile's dt, then a compensated running sum
@@ -531,7 +601,7 @@ __global__ void SS_PAIR_BOUNDS
             // own row: D skip and silu(z) gate
 #pragma unroll
             for (int i = 0; i < TL / 2; ++i) {
-                f2 o = ffma2(mk2(Dd, Dd), pair_at(uw, i, Tin()), mk2(out[2 * i], out[2 * i + 1]));
+                f2 o = ffma2(mk2(Dd, Dd), u_at(i), mk2(out[2 * i], out[2 * i + 1]));
                 if (has_z)
                     o = fmul2(o, (SS_PAIR_TANH && sizeof(Tin) == 2) ? silu2_tanh(pair_at(zw, i, Tin()))
                                                                    : silu2(pair_at(zw, i, Tin())));
@@ -620,11 +690,11 @@ int resident_ctas(K kern, int smem, int *out) {
     return SS_OK;
 }
 
-template <typename Tin, typename Tout, int TL, int S, int MODE>
+template <typename Tin, typename Tout, int TL, int S, int MODE, bool CV>
 int launch_mode(const ssh::ScanParams &p, const ssh::PairWork &w, const PairSched &sch,
                 const CUtensorMap &tm, long long units, cudaStream_t st) {
     using LY = PairLayout<Tin, TL, S>;
-    auto kern = scan_pair_kernel<Tin, Tout, TL, S, MODE>;
+    auto kern = scan_pair_kernel<Tin, Tout, TL, S, MODE, CV>;
     int per_sm = 0;
     int rc = resident_ctas(kern, LY::TOTAL, &per_sm);
     if (rc != SS_OK) return rc;
@@ -639,7 +709,7 @@ int launch_mode(const ssh::ScanParams &p, const ssh::PairWork &w, const PairSche
     return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
-template <typename Tin, typename Tout, int TL, int S>
+template <typename Tin, typename Tout, int TL, int S, bool CV>
 int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st) {
     const long long L = p.seqlen;
     // 1. pack B/C, reset the work counters
@@ -675,10 +745,10 @@ int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st
     sch.sdt = w.sdt;
     if (!w.chunked || sch.n_seg < 2) {
         // 2. one chained pass: at most one range per row block
-        return launch_mode<Tin, Tout, TL, S, kChain>(p, w, sch, tm, (long long)sch.total_rb, st);
+        return launch_mode<Tin, Tout, TL, S, kChain, CV>(p, w, sch, tm, (long long)sch.total_rb, st);
     }
     // 2. aggregate every segment but the last, in parallel
-    int rc = launch_mode<Tin, Tout, TL, S, kAgg>(p, w, sch, tm,
+    int rc = launch_mode<Tin, Tout, TL, S, kAgg, CV>(p, w, sch, tm,
                                                  (long long)sch.total_rb * (sch.n_seg - 1), st);
     if (rc != SS_OK) return rc;
     // 3. combine the segment maps along time: the state entering each segment
@@ -688,7 +758,7 @@ int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st
         if (cudaPeekAtLastError() != cudaSuccess) return SS_ERR_CUDA;
     }
     // 4. every segment again from its carried-in state, writing y
-    return launch_mode<Tin, Tout, TL, S, kSeg>(p, w, sch, tm,
+    return launch_mode<Tin, Tout, TL, S, kSeg, CV>(p, w, sch, tm,
                                                (long long)sch.total_rb * sch.n_seg, st);
 }
 
@@ -724,11 +794,20 @@ bool ssh::pair_supported(const ssh::ScanParams &p) {
     return encode_fn() != nullptr;
 }
 
-int ssh::launch_pair(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st) {
+template <bool CV>
+int launch_pair_t(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st) {
     constexpr int TL = SS_PAIR_TL, S = SS_PAIR_S;
     const bool ib = p.in_dtype == SS_BF16, ob = p.out_dtype == SS_BF16;
-    if (ib && ob) return launch_cfg<uint16_t, uint16_t, TL, S>(p, w, st);
-    if (ib) return launch_cfg<uint16_t, float, TL, S>(p, w, st);
-    if (ob) return launch_cfg<float, uint16_t, TL, S>(p, w, st);
-    return launch_cfg<float, float, TL, S>(p, w, st);
+    if (ib && ob) return launch_cfg<uint16_t, uint16_t, TL, S, CV>(p, w, st);
+    if (ib) return launch_cfg<uint16_t, float, TL, S, CV>(p, w, st);
+    if (ob) return launch_cfg<float, uint16_t, TL, S, CV>(p, w, st);
+    return launch_cfg<float, float, TL, S, CV>(p, w, st);
+}
+
+int ssh::launch_pair(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st) {
+    if (p.conv_width > 0) {
+        if (p.conv_width < 2 || p.conv_width > 4 || !p.conv_w) return SS_ERR_UNSUPPORTED;
+        return launch_pair_t<true>(p, w, st);
+    }
+    return launch_pair_t<false>(p, w, st);
 }

@@ -36,7 +36,8 @@ def test_struct_layout_matches_binding(built, tmp_path):
     import selective_state_space_136_b300 as ss
     structs = {"ss_scan_args": ss.ScanArgs, "ss_update_args": ss.UpdateArgs,
                "ss_scan_bwd_args": ss.ScanBwdArgs, "ss_ssd_args": ss.SsdArgs,
-               "ss_conv1d_args": ss.Conv1dArgs, "ss_conv1d_update_args": ss.Conv1dUpdateArgs}
+               "ss_conv1d_args": ss.Conv1dArgs, "ss_conv1d_update_args": ss.Conv1dUpdateArgs,
+               "ss_conv_scan_args": ss.ConvScanArgs}
     prog = tmp_path / "layout.c"
     body = ['#include <stdio.h>', '#include <stddef.h>', '#include "ss_scan.h"', "int main(void){"]
     for cname, cls in structs.items():
@@ -89,6 +90,7 @@ def test_host_validation_without_gpu(built):
     assert L.ss_ssd_fwd(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_conv1d_update(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_scan_fwd_noalloc(None, None, None) == ss.SS_ERR_INVALID_ARG
+    assert L.ss_conv_scan_fwd(None, None, None) == ss.SS_ERR_INVALID_ARG
     assert L.ss_set_option(None, 0, 0) == ss.SS_ERR_INVALID_ARG
     assert L.ss_destroy(None) == ss.SS_OK
     assert ss.status_string(ss.SS_ERR_TIMEOUT) == "device wait timed out"
