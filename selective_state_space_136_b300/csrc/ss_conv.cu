@@ -122,7 +122,18 @@ __global__ void __launch_bounds__(256) conv1d_chunk_kernel(const ssh::ConvParams
                 const int j = i - (W - 1) + k;  // input index within the chunk
                 acc = fmaf(w[k], j >= 0 ? cur[u][j] : prev[u][4 + j], acc);
             }
-            o[i] = p.silu ? silu(acc) : acc;
+            o[i] = acc;
+        }
+        if (p.silu) {
+            // bf16 outputs: silu through one tanh.approx (relative error near
+            // 2^-11, below the 2^-9 rounding of the bf16 result); fp32
+            // outputs: z / (1 + 2^(-z log2 e))
+#pragma unroll
+            for (int i = 0; i < kChunk; i += 2) {
+                const f2 z2 = mk2(o[i], o[i + 1]);
+                const f2 s2 = sizeof(Tout) == 2 ? silu2_tanh(z2) : mk2(silu(o[i]), silu(o[i + 1]));
+                o[i] = s2.x, o[i + 1] = s2.y;
+            }
         }
         store8(static_cast<Tout *>(p.out) + (long long)r * L + (long long)c * kChunk, o);
         if (p.final_state && c == cpr - 1) {
