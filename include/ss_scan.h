@@ -383,9 +383,11 @@ const char *ss_status_string(int status);
  *                           SS_DISC_ZOH uses the exact zero-order hold
  *                           (exp(dt A) - 1) / A * B of the Mamba page's section
  *                           "Method" (dt * B where A = 0). ZOH runs on the
- *                           one-thread-per-row kernels only: AUTO picks them,
- *                           and forcing the pair, split-row or chunked kernels
- *                           returns SS_ERR_UNSUPPORTED. ss_scan_fwd_noalloc
+ *                           chained pair-row and chunked kernels (AUTO picks
+ *                           them as for the simplified form) and on the
+ *                           one-thread-per-row kernels; forcing the 4-thread
+ *                           split-row kernel (THREADS_PER_ROW 4) returns
+ *                           SS_ERR_UNSUPPORTED, and so does ss_conv_scan_fwd. ss_scan_fwd_noalloc
  *                           always uses the simplified form.
  *   SS_OPT_TEST_DROP_TILE   test hook: the rows kernel never issues the loads
  *                           of this tile index, so its wait runs out and the

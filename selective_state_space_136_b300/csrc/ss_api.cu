@@ -298,8 +298,9 @@ bool prefer_chunked(const ss_ctx *ctx, const ssh::ScanParams &p) {
 int dispatch_scan(ss_ctx *ctx, const ssh::ScanParams &p, cudaStream_t st) {
     int variant = ctx->variant;
     const bool rows_ok = ssh::rows_supported(p) && ssh::seq_supported(p);
-    // the exact zero-order hold runs on the one-thread-per-row kernels only
-    const bool pair_ok = ssh::pair_supported(p) && !ctx->zoh;
+    // the exact zero-order hold runs on the pair-row kernels (chained and
+    // chunked) and the one-thread-per-row kernels; not on the 4-thread rows kernel
+    const bool pair_ok = ssh::pair_supported(p);
     if (variant == SS_VARIANT_AUTO) {
         // few row blocks for the machine: scan time segments in parallel
         if (pair_ok && prefer_chunked(ctx, p)) variant = SS_VARIANT_CHUNKED;
@@ -313,7 +314,7 @@ int dispatch_scan(ss_ctx *ctx, const ssh::ScanParams &p, cudaStream_t st) {
     } else if (variant == SS_VARIANT_ROWS) {
         int tpr = ctx->rows_tpr;
         if (tpr == 0) tpr = pair_ok ? 2 : 1;
-        if (ctx->zoh && tpr != 1) return SS_ERR_UNSUPPORTED;
+        if (ctx->zoh && tpr == 4) return SS_ERR_UNSUPPORTED;
         if (tpr == 2) {
             if (!pair_ok) return SS_ERR_UNSUPPORTED;
             rc = run_pair(ctx, p, false, st, &launches);

@@ -236,6 +236,25 @@ __global__ void __launch_bounds__(128) carry_combine_kernel(const ssh::ScanParam
     }
 }
 
+
+// Input term of one state pair under the exact zero-order hold, for decay
+// exponent tt = dt a log2(e) (e = 2^tt), 1 / a and u B: ((e - 1) / a) u B.
+// For |dt a| < 1/8 the difference e - 1 cancels, so there the factor is
+// dt (1 + x/2 + x^2/6 + x^3/24 + x^4/120), x = dt a (Taylor series of
+// (e^x - 1) / x, truncation below x^5/720 < 5e-9 relative); an a of 0 has
+// x = 0 and gets dt, the limit.
+__device__ __forceinline__ f2 zoh_input(f2 tt, f2 e, f2 ia, f2 dd, f2 ub) {
+    const f2 fd = ffma2(e, ia, mk2(-ia.x, -ia.y));
+    const f2 x = fmul2(tt, mk2(kLn2, kLn2));
+    f2 ph = ffma2(x, mk2(1.f / 120.f, 1.f / 120.f), mk2(1.f / 24.f, 1.f / 24.f));
+    ph = ffma2(ph, x, mk2(1.f / 6.f, 1.f / 6.f));
+    ph = ffma2(ph, x, mk2(0.5f, 0.5f));
+    ph = ffma2(ph, x, mk2(1.f, 1.f));
+    const f2 fs = fmul2(dd, ph);
+    const f2 f = mk2(fabsf(x.x) < 0.125f ? fs.x : fd.x, fabsf(x.y) < 0.125f ? fs.y : fd.y);
+    return fmul2(f, ub);
+}
+
 // ---------------------------------------------------------------- the scan
 
 // MODE: kChain  - units chained along time through the carry buffer (one pass);
@@ -244,17 +263,23 @@ __global__ void __launch_bounds__(128) carry_combine_kernel(const ssh::ScanParam
 //       kSeg    - output pass: every segment from its carried-in state.
 enum { kChain = 0, kAgg = 1, kSeg = 2 };
 
+// what the kernel does besides the plain recurrence:
+//  kConv - the causal convolution fused in front (u formed from x in registers)
+//  kZoh  - the exact zero-order-hold input factor (exp(dt a) - 1) / a in place of dt
+enum { kPlain = 0, kConv = 1, kZoh = 2 };
+
 #ifdef SS_PAIR_MAXNREG
 #define SS_PAIR_BOUNDS __maxnreg__(SS_PAIR_MAXNREG)
 #else
 #define SS_PAIR_BOUNDS __launch_bounds__(32, SS_PAIR_MINB)
 #endif
 
-template <typename Tin, typename Tout, int TL, int S, int MODE, bool CV>
+template <typename Tin, typename Tout, int TL, int S, int MODE, int FL>
 __global__ void SS_PAIR_BOUNDS
     scan_pair_kernel(const __grid_constant__ CUtensorMap tm_bc, const ssh::ScanParams p,
                      const PairSched sch) {
     constexpr bool OUT = MODE != kAgg;  // produces y
+    constexpr bool CV = FL == kConv, ZH = FL == kZoh;
     using LY = PairLayout<Tin, TL, S>;
     constexpr unsigned FULL = 0xffffffffu;
 
@@ -330,6 +355,17 @@ __global__ void SS_PAIR_BOUNDS
             const int n = 8 * q + 2 * j;
             A2[0][j] = mk2(p.A[(long long)dc * kN + n] * kLog2e, p.A[(long long)dc * kN + n + 1] * kLog2e);
             A2[1][j] = mk2(p.A[(long long)dp * kN + n] * kLog2e, p.A[(long long)dp * kN + n + 1] * kLog2e);
+        }
+        // exact zero-order hold: 1 / a per state (an a of 0 is covered by the
+        // series form below, which the factor then always selects)
+        f2 ia[2][ZH ? 4 : 1];
+        if constexpr (ZH) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = 8 * q + 2 * j;
+                ia[0][j] = mk2(1.f / p.A[(long long)dc * kN + n], 1.f / p.A[(long long)dc * kN + n + 1]);
+                ia[1][j] = mk2(1.f / p.A[(long long)dp * kN + n], 1.f / p.A[(long long)dp * kN + n + 1]);
+            }
         }
         // initial state: zero (aggregate pass), h0 (first segment), the
         // carried-in state of the combine pass, or the chained carry
@@ -503,7 +539,9 @@ __global__ void SS_PAIR_BOUNDS
             for (int i = 0; i < TL / 2; ++i) {
                 const f2 x = fadd2(pair_at(dw, i, Tin()), mk2(bias, bias));
                 dt[i] = p.softplus ? softplus2_d6(x) : x;
-                du[i] = fmul2(dt[i], u_at(i));
+                // the simplified input matrix takes dt * u; the zero-order hold
+                // takes u (its factor is formed per state)
+                du[i] = ZH ? u_at(i) : fmul2(dt[i], u_at(i));
             }
             if (MODE == kAgg) {
                 // pairwise sum of the tile's dt, then a compensated running sum
@@ -554,7 +592,10 @@ __global__ void SS_PAIR_BOUNDS
                         for (int j = 0; j < 4; ++j) {
                             const f2 tt = fmul2(dd, A2[r][j]);
                             const f2 e = mk2(ex2(tt.x), ex2(tt.y));
-                            h[r][j] = ffma2(e, h[r][j], fmul2(uu, Bp[j]));
+                            if constexpr (ZH)
+                                h[r][j] = ffma2(e, h[r][j], zoh_input(tt, e, ia[r][j], dd, fmul2(uu, Bp[j])));
+                            else
+                                h[r][j] = ffma2(e, h[r][j], fmul2(uu, Bp[j]));
                         }
                     }
                 }
@@ -580,7 +621,10 @@ __global__ void SS_PAIR_BOUNDS
                     for (int j = 0; j < 4; ++j) {
                         const f2 tt = fmul2(dd, A2[r][j]);
                         const f2 e = mk2(ex2(tt.x), ex2(tt.y));
-                        h[r][j] = ffma2(e, h[r][j], fmul2(uu, Bp[j]));
+                        if constexpr (ZH)
+                            h[r][j] = ffma2(e, h[r][j], zoh_input(tt, e, ia[r][j], dd, fmul2(uu, Bp[j])));
+                        else
+                            h[r][j] = ffma2(e, h[r][j], fmul2(uu, Bp[j]));
                         if (j == 0) a0 = fmul2(Cp[0], h[r][0]);
                         else if (j == 1) a1 = fmul2(Cp[1], h[r][1]);
                         else if (j == 2) a0 = ffma2(Cp[2], h[r][2], a0);
@@ -690,11 +734,11 @@ int resident_ctas(K kern, int smem, int *out) {
     return SS_OK;
 }
 
-template <typename Tin, typename Tout, int TL, int S, int MODE, bool CV>
+template <typename Tin, typename Tout, int TL, int S, int MODE, int FL>
 int launch_mode(const ssh::ScanParams &p, const ssh::PairWork &w, const PairSched &sch,
                 const CUtensorMap &tm, long long units, cudaStream_t st) {
     using LY = PairLayout<Tin, TL, S>;
-    auto kern = scan_pair_kernel<Tin, Tout, TL, S, MODE, CV>;
+    auto kern = scan_pair_kernel<Tin, Tout, TL, S, MODE, FL>;
     int per_sm = 0;
     int rc = resident_ctas(kern, LY::TOTAL, &per_sm);
     if (rc != SS_OK) return rc;
@@ -709,7 +753,7 @@ int launch_mode(const ssh::ScanParams &p, const ssh::PairWork &w, const PairSche
     return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
-template <typename Tin, typename Tout, int TL, int S, bool CV>
+template <typename Tin, typename Tout, int TL, int S, int FL>
 int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st) {
     const long long L = p.seqlen;
     // 1. pack B/C, reset the work counters
@@ -745,10 +789,10 @@ int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st
     sch.sdt = w.sdt;
     if (!w.chunked || sch.n_seg < 2) {
         // 2. one chained pass: at most one range per row block
-        return launch_mode<Tin, Tout, TL, S, kChain, CV>(p, w, sch, tm, (long long)sch.total_rb, st);
+        return launch_mode<Tin, Tout, TL, S, kChain, FL>(p, w, sch, tm, (long long)sch.total_rb, st);
     }
     // 2. aggregate every segment but the last, in parallel
-    int rc = launch_mode<Tin, Tout, TL, S, kAgg, CV>(p, w, sch, tm,
+    int rc = launch_mode<Tin, Tout, TL, S, kAgg, FL>(p, w, sch, tm,
                                                  (long long)sch.total_rb * (sch.n_seg - 1), st);
     if (rc != SS_OK) return rc;
     // 3. combine the segment maps along time: the state entering each segment
@@ -758,7 +802,7 @@ int launch_cfg(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st
         if (cudaPeekAtLastError() != cudaSuccess) return SS_ERR_CUDA;
     }
     // 4. every segment again from its carried-in state, writing y
-    return launch_mode<Tin, Tout, TL, S, kSeg, CV>(p, w, sch, tm,
+    return launch_mode<Tin, Tout, TL, S, kSeg, FL>(p, w, sch, tm,
                                                (long long)sch.total_rb * sch.n_seg, st);
 }
 
@@ -794,20 +838,22 @@ bool ssh::pair_supported(const ssh::ScanParams &p) {
     return encode_fn() != nullptr;
 }
 
-template <bool CV>
+template <int FL>
 int launch_pair_t(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st) {
     constexpr int TL = SS_PAIR_TL, S = SS_PAIR_S;
     const bool ib = p.in_dtype == SS_BF16, ob = p.out_dtype == SS_BF16;
-    if (ib && ob) return launch_cfg<uint16_t, uint16_t, TL, S, CV>(p, w, st);
-    if (ib) return launch_cfg<uint16_t, float, TL, S, CV>(p, w, st);
-    if (ob) return launch_cfg<float, uint16_t, TL, S, CV>(p, w, st);
-    return launch_cfg<float, float, TL, S, CV>(p, w, st);
+    if (ib && ob) return launch_cfg<uint16_t, uint16_t, TL, S, FL>(p, w, st);
+    if (ib) return launch_cfg<uint16_t, float, TL, S, FL>(p, w, st);
+    if (ob) return launch_cfg<float, uint16_t, TL, S, FL>(p, w, st);
+    return launch_cfg<float, float, TL, S, FL>(p, w, st);
 }
 
 int ssh::launch_pair(const ssh::ScanParams &p, const ssh::PairWork &w, cudaStream_t st) {
     if (p.conv_width > 0) {
-        if (p.conv_width < 2 || p.conv_width > 4 || !p.conv_w) return SS_ERR_UNSUPPORTED;
-        return launch_pair_t<true>(p, w, st);
+        // the fused convolution serves the simplified input matrix only
+        if (p.conv_width < 2 || p.conv_width > 4 || !p.conv_w || p.zoh) return SS_ERR_UNSUPPORTED;
+        return launch_pair_t<kConv>(p, w, st);
     }
-    return launch_pair_t<false>(p, w, st);
+    if (p.zoh) return launch_pair_t<kZoh>(p, w, st);
+    return launch_pair_t<kPlain>(p, w, st);
 }

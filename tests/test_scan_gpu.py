@@ -373,18 +373,30 @@ def test_device_wait_times_out_cleanly(tpr, drop):
 
 # ---------------------------------------------------------------- exact zero-order hold
 
-@pytest.mark.parametrize("N,L,dt", [(16, 256, "bf16"), (16, 100, "f32"), (4, 64, "f32"),
-                                    (16, 2048, "bf16")])
-def test_zoh_scan(N, L, dt):
-    """SS_DISC_ZOH: the input matrix (exp(dt A) - 1) / A * B, against the oracle's ZOH."""
+ZOH_VARIANTS = [("auto", ss.SS_VARIANT_AUTO, 0, 0), ("chained", ss.SS_VARIANT_ROWS, 2, 0),
+                ("chunked", ss.SS_VARIANT_CHUNKED, 0, 3), ("seq", ss.SS_VARIANT_ROWS, 1, 0),
+                ("simple", ss.SS_VARIANT_SIMPLE, 0, 0)]
+
+
+@pytest.mark.parametrize("N,L,dt", [(16, 256, "bf16"), (16, 256, "f32"), (16, 100, "f32"),
+                                    (4, 64, "f32"), (16, 2048, "bf16")])
+@pytest.mark.parametrize("name,variant,tpr,segments", ZOH_VARIANTS, ids=[v[0] for v in ZOH_VARIANTS])
+def test_zoh_scan(N, L, dt, name, variant, tpr, segments):
+    """SS_DISC_ZOH: the input matrix (exp(dt A) - 1) / A * B, against the
+    oracle's ZOH, on every kernel that takes it (the pair-row kernels only
+    where their shape rules hold: dstate 16, L a multiple of 16)."""
+    pair = name in ("chained", "chunked")
+    if pair and (N != 16 or L % 16):
+        pytest.skip("the pair-row kernels take dstate 16 and whole 16-step tiles")
     cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=2, dim=64, dstate=N, seqlen=L,
                            in_dtype=dt, seed=90 + N + L)
     inp = workloads.scan_inputs(cfg, with_h0=True)
     t = device_inputs(inp, cfg)
-    ctx = _ctx()
+    ctx = _ctx(variant, tpr, segments)
     ctx.set_option(ss.SS_OPT_DISCRETIZATION, ss.SS_DISC_ZOH)
     y, hl = _run(cfg, t, ctx, h0=t["h0"])
-    assert ctx.last_launch()[0] in (ss.SS_VARIANT_ROWS, ss.SS_VARIANT_SIMPLE)
+    if pair:
+        assert ctx.last_launch()[0] == variant
     rows = np.arange(cfg.rows)
     A = inp["A"]
     y_ref, h_ref = oracle.scan_fwd(inp["u"], inp["delta"], A, inp["B"], inp["C"], D=inp["D"],
@@ -397,13 +409,37 @@ def test_zoh_scan(N, L, dt):
     assert np.max(np.abs(y_s - y_ref)) > 1e-3 * np.max(np.abs(y_ref))
 
 
-def test_zoh_forced_fast_kernels_unsupported():
+def test_zoh_small_and_zero_decay_rates():
+    """ZOH where dt a is tiny (the series branch of the pair kernels) and
+    exactly zero (A = 0: the factor is dt), fp32 inputs against the oracle."""
+    cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=1, dim=64, seqlen=128,
+                           in_dtype="f32", seed=97)
+    inp = workloads.scan_inputs(cfg, with_h0=True)
+    A = inp["A"].copy()
+    A[:, 0] = 0.0                    # no decay at all
+    A[:, 1] = -1e-4                  # dt a far inside the series range
+    A[:, 2] = -0.125 / 0.05          # near the switch for typical dt
+    inp["A"] = A
+    t = device_inputs(inp, cfg)
+    for variant, tpr, seg in ((ss.SS_VARIANT_ROWS, 2, 0), (ss.SS_VARIANT_CHUNKED, 0, 2)):
+        ctx = _ctx(variant, tpr, seg)
+        ctx.set_option(ss.SS_OPT_DISCRETIZATION, ss.SS_DISC_ZOH)
+        y, hl = _run(cfg, t, ctx, h0=t["h0"])
+        rows = np.arange(cfg.rows)
+        y_ref, h_ref = oracle.scan_fwd(inp["u"], inp["delta"], A, inp["B"], inp["C"], D=inp["D"],
+                                       delta_bias=inp["delta_bias"], z=inp["z"], h0=inp["h0"],
+                                       rows=rows, dim=cfg.dim, zoh=True)
+        check_close(y.reshape(cfg.rows, -1), y_ref, False, "y")
+        check_close(hl.reshape(cfg.rows, -1), h_ref, False, "h_last")
+
+
+def test_zoh_split_row_kernel_unsupported():
+    """The 4-thread split-row kernel does not take the zero-order hold."""
     cfg = workloads.scaled(workloads.CONFIGS["mamba2p8b"], batch=1, dim=64, seqlen=256, seed=95)
     inp = workloads.scan_inputs(cfg)
     t = device_inputs(inp, cfg)
-    for variant, tpr in ((ss.SS_VARIANT_ROWS, 2), (ss.SS_VARIANT_ROWS, 4), (ss.SS_VARIANT_CHUNKED, 0)):
-        ctx = _ctx(variant, tpr)
-        ctx.set_option(ss.SS_OPT_DISCRETIZATION, ss.SS_DISC_ZOH)
-        with pytest.raises(ss.SSError) as ei:
-            _run(cfg, t, ctx)
-        assert ei.value.status == ss.SS_ERR_UNSUPPORTED
+    ctx = _ctx(ss.SS_VARIANT_ROWS, 4)
+    ctx.set_option(ss.SS_OPT_DISCRETIZATION, ss.SS_DISC_ZOH)
+    with pytest.raises(ss.SSError) as ei:
+        _run(cfg, t, ctx)
+    assert ei.value.status == ss.SS_ERR_UNSUPPORTED
