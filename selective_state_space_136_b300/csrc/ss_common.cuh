@@ -142,6 +142,21 @@ __device__ __forceinline__ f2 log1p_unit2_d6(f2 w) {
     p = ffma2(p, w, mk2(9.999987483e-01f, 9.999987483e-01f));
     return fmul2(p, w);
 }
+// Degree-4 variant (within 5.7e-5 relative of log1p(w)): for bf16 inputs,
+// whose own rounding (2^-9 relative) is far coarser.
+__device__ __forceinline__ f2 log1p_unit2_d4(f2 w) {
+    f2 p = mk2(4.134725779e-02f, 4.134725779e-02f);
+    p = ffma2(p, w, mk2(-1.574271172e-01f, -1.574271172e-01f));
+    p = ffma2(p, w, mk2(3.063008785e-01f, 3.063008785e-01f));
+    p = ffma2(p, w, mk2(-4.969778061e-01f, -4.969778061e-01f));
+    p = ffma2(p, w, mk2(9.999432564e-01f, 9.999432564e-01f));
+    return fmul2(p, w);
+}
+__device__ __forceinline__ f2 softplus2_d4(f2 x) {
+    const f2 t = fmul2(mk2(fabsf(x.x), fabsf(x.y)), mk2(-kLog2e, -kLog2e));
+    const f2 w = mk2(ex2(t.x), ex2(t.y));
+    return fadd2(mk2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), log1p_unit2_d4(w));
+}
 __device__ __forceinline__ f2 softplus2_d6(f2 x) {
     const f2 t = fmul2(mk2(fabsf(x.x), fabsf(x.y)), mk2(-kLog2e, -kLog2e));
     const f2 w = mk2(ex2(t.x), ex2(t.y));

@@ -538,7 +538,8 @@ __global__ void SS_PAIR_BOUNDS
 #pragma unroll
             for (int i = 0; i < TL / 2; ++i) {
                 const f2 x = fadd2(pair_at(dw, i, Tin()), mk2(bias, bias));
-                dt[i] = p.softplus ? softplus2_d6(x) : x;
+                // softplus: the degree-4 fit for bf16 inputs, degree 6 for fp32
+                dt[i] = p.softplus ? (sizeof(Tin) == 2 ? softplus2_d4(x) : softplus2_d6(x)) : x;
                 // the simplified input matrix takes dt * u; the zero-order hold
                 // takes u (its factor is formed per state)
                 du[i] = ZH ? u_at(i) : fmul2(dt[i], u_at(i));
@@ -616,7 +617,7 @@ __global__ void SS_PAIR_BOUNDS
                 for (int r = 0; r < 2; ++r) {
                     const float dtr = r ? dtp : dto, dur = r ? dup : duo;
                     const f2 dd = mk2(dtr, dtr), uu = mk2(dur, dur);
-                    f2 a0, a1;
+                    f2 a;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const f2 tt = fmul2(dd, A2[r][j]);
@@ -625,12 +626,9 @@ __global__ void SS_PAIR_BOUNDS
                             h[r][j] = ffma2(e, h[r][j], zoh_input(tt, e, ia[r][j], dd, fmul2(uu, Bp[j])));
                         else
                             h[r][j] = ffma2(e, h[r][j], fmul2(uu, Bp[j]));
-                        if (j == 0) a0 = fmul2(Cp[0], h[r][0]);
-                        else if (j == 1) a1 = fmul2(Cp[1], h[r][1]);
-                        else if (j == 2) a0 = ffma2(Cp[2], h[r][2], a0);
-                        else a1 = ffma2(Cp[3], h[r][3], a1);
+                        // one accumulator chain over the 4 pairs (even and odd states)
+                        a = j == 0 ? fmul2(Cp[0], h[r][0]) : ffma2(Cp[j], h[r][j], a);
                     }
-                    const f2 a = fadd2(a0, a1);
                     part[r] = a.x + a.y;
                 }
                 // own total = my half of my row + the partner's half of my row
