@@ -225,6 +225,21 @@ def probe_alu(device):
         r, g = ctypes.c_double(), ctypes.c_double()
         rc = lib.ss_probe_alu(which, device, ctypes.byref(r), ctypes.byref(g))
         out[name] = {"ops_per_s": r.value, "sm_ghz": g.value, "rc": rc}
+    # the scan's inner step without memory traffic, at the parallelism shapes
+    # allow: 2 rows per lane pair with 8 warps per SM (32-row warps: the 2.8B
+    # shape's 40960 rows fill 1184 warps once), 4 rows per lane pair with 4 or
+    # 8 warps per SM (64-row warps)
+    lib.ss_probe_scan_step.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.POINTER(ctypes.c_double),
+                                       ctypes.POINTER(ctypes.c_double)]
+    steps = {}
+    for rows, warps in ((2, 8), (2, 16), (4, 4), (4, 8)):
+        r, g = ctypes.c_double(), ctypes.c_double()
+        rc = lib.ss_probe_scan_step(rows, warps, device, ctypes.byref(r), ctypes.byref(g))
+        steps["rows%d_warps%d" % (rows, warps)] = {
+            "elements_per_clk_per_sm": r.value, "frac_of_ex2_peak": r.value / 32.0,
+            "sm_ghz": g.value, "rc": rc}
+    out["scan_step"] = steps
     return out
 
 
