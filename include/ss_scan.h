@@ -151,8 +151,11 @@ int ss_state_update(ss_ctx *ctx, const ss_update_args *args, ss_stream_t stream)
  *                  NULL when z is NULL)
  *     dA         : (dim, dstate);  dB, dC: (batch, dstate, seqlen)
  *     dD, ddelta_bias : (dim) or NULL;  dh0: (batch, dim, dstate) or NULL
- *   seqlen must be a multiple of 16 and the discretization SS_DISC_SIMPLIFIED,
- *   else SS_ERR_UNSUPPORTED. Outputs must not overlap inputs or each other.
+ *   The context's SS_OPT_DISCRETIZATION applies: with SS_DISC_ZOH the
+ *   gradients are those of the exact zero-order-hold scan (taken on the
+ *   one-lane-per-state kernel, which is slower than the simplified form's).
+ *   seqlen must be a multiple of 16, else SS_ERR_UNSUPPORTED. Outputs must not
+ *   overlap inputs or each other.
  *   dB and dC are sums over channels accumulated with atomic adds, so their
  *   low bits may differ from run to run.
  */
@@ -377,7 +380,7 @@ const char *ss_status_string(int status);
  *   SS_OPT_WAIT_LIMIT       polls before a device-side wait gives up and
  *                           reports SS_ERR_TIMEOUT (default 2^22, roughly a
  *                           second; 1 .. 2^30).
- *   SS_OPT_DISCRETIZATION   input matrix of ss_scan_fwd and ss_state_update:
+ *   SS_OPT_DISCRETIZATION   input matrix of ss_scan_fwd, ss_scan_bwd and ss_state_update:
  *                           SS_DISC_SIMPLIFIED (default) uses dt * B, the step
  *                           the soft186.com article prints ("动态参数化的状态空间");
  *                           SS_DISC_ZOH uses the exact zero-order hold

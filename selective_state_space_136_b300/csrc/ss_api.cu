@@ -500,11 +500,10 @@ int ss_scan_bwd(ss_ctx *ctx, const ss_scan_bwd_args *a, ss_stream_t stream) {
         for (size_t j = i + 1; j < n_out; ++j)
             if (overlaps(outs[i], outs[j])) return SS_ERR_INVALID_ARG;
     }
-    if (ctx->zoh) return SS_ERR_UNSUPPORTED;
     ssh::BwdParams p{a->batch, a->dim, a->dstate, a->seqlen, a->in_dtype, a->u, a->delta, a->z,
                      a->A, a->B, a->C, a->D, a->delta_bias, a->delta_softplus, a->h0, a->dy,
                      a->dh_last, a->du, a->ddelta, a->dz, a->dA, a->dB, a->dC, a->dD,
-                     a->ddelta_bias, a->dh0, nullptr};
+                     a->ddelta_bias, a->dh0, nullptr, ctx->zoh};
     if (!ssh::bwd_supported(p)) return SS_ERR_UNSUPPORTED;
     if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
     const size_t need = ssh::bwd_ckpt_bytes(p);

@@ -9,6 +9,13 @@
 // recomputes each half tile's 8 states into shared memory from its checkpoint
 // and walks them backwards.
 //
+// With the exact zero-order hold the input term is f_n B_n u with
+// f_n = (e_n - 1) / A_n; then dB_n(t) += g_n f_n u, du takes g_n f_n B_n, ddt
+// takes g_n (A_n e_n h_n(t-1) + e_n B_n u) (df/ddt = e), and dA_n takes
+// g_n (dt e_n h_n(t-1) + (dt e_n - f_n) / A_n B_n u). Where |dt A| < 1/8 both
+// f and df/dA come from their Taylor series in x = dt A (the differences
+// cancel there): f = dt phi(x), df/dA = dt^2 phi'(x), phi(x) = (e^x - 1) / x.
+//
 // Reverse step t of a row (g = dL/dh(t), the adjoint state, in registers):
 //     s = sum_n C_n h_n(t) + D u,  gs = dy silu(z),  dz = dy s silu'(z)
 //     g_n += gs C_n;   dC_n(t) += gs h_n(t);   dB_n(t) += g_n dt u
@@ -85,7 +92,52 @@ __device__ __forceinline__ void load_bc(BwdSmem<N> &sm, const ssh::BwdParams &p,
     __syncwarp();
 }
 
-template <typename Tin, int N>
+// Zero-order-hold input factor f = (e^x - 1) / a and its derivative in a,
+// given x = dt a, e = e^x and ia = 1 / a (any value where a = 0: x is 0 there
+// and the series is taken). Series: phi(x) = (e^x - 1) / x = sum x^k / (k+1)!
+// and phi'(x) = sum (k+1) x^k / (k+2)!, five terms each (relative truncation
+// below 5e-8 for |x| < 1/8).
+__device__ __forceinline__ float zoh_phi(float x) {
+    return fmaf(fmaf(fmaf(fmaf(x, 1.f / 120.f, 1.f / 24.f), x, 1.f / 6.f), x, 0.5f), x, 1.f);
+}
+__device__ __forceinline__ float zoh_dphi(float x) {
+    return fmaf(fmaf(fmaf(fmaf(x, 1.f / 144.f, 1.f / 30.f), x, 0.125f), x, 1.f / 3.f), x, 0.5f);
+}
+__device__ __forceinline__ float zoh_factor(float dt, float x, float e, float ia, float *fa) {
+    if (fabsf(x) < 0.125f) {
+        *fa = dt * dt * zoh_dphi(x);
+        return dt * zoh_phi(x);
+    }
+    const float f = (e - 1.f) * ia;
+    *fa = (dt * e - f) * ia;
+    return f;
+}
+// Both states of a pair in packed arithmetic, both forms evaluated and one
+// taken per state (no divergent branch); dsq = dt^2. The forward steps need f
+// alone.
+__device__ __forceinline__ f2 zoh_pick(f2 x, f2 series, f2 exact) {
+    return mk2(fabsf(x.x) < 0.125f ? series.x : exact.x, fabsf(x.y) < 0.125f ? series.y : exact.y);
+}
+__device__ __forceinline__ f2 zoh_f2(f2 dd, f2 x, f2 e, f2 ia) {
+    f2 ph = ffma2(x, mk2(1.f / 120.f, 1.f / 120.f), mk2(1.f / 24.f, 1.f / 24.f));
+    ph = ffma2(ph, x, mk2(1.f / 6.f, 1.f / 6.f));
+    ph = ffma2(ph, x, mk2(0.5f, 0.5f));
+    ph = ffma2(ph, x, mk2(1.f, 1.f));
+    return zoh_pick(x, fmul2(dd, ph), ffma2(e, ia, mk2(-ia.x, -ia.y)));
+}
+__device__ __forceinline__ f2 zoh_factor2(f2 dd, f2 dsq, f2 x, f2 e, f2 ia, f2 *fa) {
+    const f2 f = zoh_f2(dd, x, e, ia);
+    f2 dph = ffma2(x, mk2(1.f / 144.f, 1.f / 144.f), mk2(1.f / 30.f, 1.f / 30.f));
+    dph = ffma2(dph, x, mk2(0.125f, 0.125f));
+    dph = ffma2(dph, x, mk2(1.f / 3.f, 1.f / 3.f));
+    dph = ffma2(dph, x, mk2(0.5f, 0.5f));
+    // exact: (dt e - f) / a; in the series range f is already the series value
+    // and this form is not taken
+    *fa = zoh_pick(x, fmul2(dsq, dph), fmul2(ffma2(dd, e, mk2(-f.x, -f.y)), ia));
+    return f;
+}
+
+template <typename Tin, int N, bool ZH>
 __global__ void __launch_bounds__(32) scan_bwd_kernel(const ssh::BwdParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     BwdSmem<N> &sm = *reinterpret_cast<BwdSmem<N> *>(smem_raw);
@@ -121,10 +173,27 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ssh::BwdParams p) {
             dt[t] = p.softplus ? softplus1(xv[t]) : xv[t];
         }
     };
+    // one forward step; du is dt * u (simplified) or u (zero-order hold)
+    float iA[ZH ? N : 1];  // 1 / A (0 where A = 0)
+#pragma unroll
+    for (int n = 0; n < (ZH ? N : 1); ++n) {
+        const float a = p.A[(long long)dc * N + n];
+        iA[n] = a != 0.f ? 1.f / a : 0.f;
+    }
     auto fwd_step = [&](float *h, float dt, float du, int t) {
 #pragma unroll
-        for (int n = 0; n < N; ++n) h[n] = fmaf(ex2(dt * A2[n]), h[n], du * sm.bc[t][n]);
+        for (int n = 0; n < N; ++n) {
+            const float e = ex2(dt * A2[n]);
+            if constexpr (ZH) {
+                float fa;
+                const float f = zoh_factor(dt, dt * (A2[n] * kLn2), e, iA[n], &fa);
+                h[n] = fmaf(e, h[n], f * du * sm.bc[t][n]);
+            } else {
+                h[n] = fmaf(e, h[n], du * sm.bc[t][n]);
+            }
+        }
     };
+    auto step_in = [&](float dt, float u) { return ZH ? u : dt * u; };
 
     // ---- forward sweep: the state entering every tile
     float h[N];
@@ -138,7 +207,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ssh::BwdParams p) {
         float dt[kTL], uv[kTL], xv[kTL];
         tile_dt(l0, dt, uv, xv);
 #pragma unroll
-        for (int t = 0; t < kTL; ++t) fwd_step(h, dt[t], dt[t] * uv[t], t);
+        for (int t = 0; t < kTL; ++t) fwd_step(h, dt[t], step_in(dt[t], uv[t]), t);
     }
 
     // ---- reverse sweep
@@ -186,7 +255,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ssh::BwdParams p) {
 #pragma unroll
                 for (int t = 0; t < kHalf; ++t) {
                     const float dtt = sm.in[0][t][lane];
-                    fwd_step(hp, dtt, dtt * sm.in[1][t][lane], t);
+                    fwd_step(hp, dtt, step_in(dtt, sm.in[1][t][lane]), t);
                 }
             }
             {
@@ -196,7 +265,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ssh::BwdParams p) {
 #pragma unroll
                 for (int t = 0; t < kHalf; ++t) {
                     const float dtt = sm.in[0][t0 + t][lane];
-                    fwd_step(hh, dtt, dtt * sm.in[1][t0 + t][lane], t0 + t);
+                    fwd_step(hh, dtt, step_in(dtt, sm.in[1][t0 + t][lane]), t0 + t);
 #pragma unroll
                     for (int n = 0; n < N; ++n) sm.S[t][n][lane] = hh[n];
                 }
@@ -233,12 +302,23 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ssh::BwdParams p) {
                     const float e = ex2(dtt * A2[n]);
                     g[n] = fmaf(gs, Cn, g[n]);
                     v[N + n] = gs * hcur[n];
-                    const float gdu = g[n] * dtt;
-                    v[n] = gdu * u;
-                    gu_ = fmaf(gdu, Bn, gu_);
                     const float ehp = e * hprev[n];
-                    gdt = fmaf(g[n], fmaf(A2[n] * kLn2, ehp, Bn * u), gdt);
-                    gA[n] = fmaf(gdu, ehp, gA[n]);
+                    if constexpr (ZH) {
+                        const float an = A2[n] * kLn2;
+                        float fa;
+                        const float f = zoh_factor(dtt, dtt * an, e, iA[n], &fa);
+                        const float gf = g[n] * f;
+                        v[n] = gf * u;
+                        gu_ = fmaf(gf, Bn, gu_);
+                        gdt = fmaf(g[n], fmaf(an, ehp, e * Bn * u), gdt);
+                        gA[n] = fmaf(g[n], fmaf(dtt, ehp, fa * Bn * u), gA[n]);
+                    } else {
+                        const float gdu = g[n] * dtt;
+                        v[n] = gdu * u;
+                        gu_ = fmaf(gdu, Bn, gu_);
+                        gdt = fmaf(g[n], fmaf(A2[n] * kLn2, ehp, Bn * u), gdt);
+                        gA[n] = fmaf(gdu, ehp, gA[n]);
+                    }
                     g[n] *= e;
                     hcur[n] = hprev[n];
                 }
@@ -311,8 +391,8 @@ struct BwdSmem2 {
     float io[4][kTL][32];
 };
 
-template <typename Tin, int N>
-__global__ void __launch_bounds__(32, 9) scan_bwd2_kernel(const ssh::BwdParams p) {
+template <typename Tin, int N, bool ZH>
+__global__ void __launch_bounds__(32, ZH ? 8 : 9) scan_bwd2_kernel(const ssh::BwdParams p) {
     constexpr int NP = N / 2;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -331,6 +411,10 @@ __global__ void __launch_bounds__(32, 9) scan_bwd2_kernel(const ssh::BwdParams p
 #pragma unroll
     for (int j = 0; j < NP; ++j)
         Ar[j] = mk2(p.A[(long long)dc * N + 2 * j], p.A[(long long)dc * N + 2 * j + 1]);
+    f2 iA[ZH ? NP : 1];  // 1 / A (0 where A = 0)
+#pragma unroll
+    for (int j = 0; j < (ZH ? NP : 1); ++j)
+        iA[j] = mk2(Ar[j].x != 0.f ? 1.f / Ar[j].x : 0.f, Ar[j].y != 0.f ? 1.f / Ar[j].y : 0.f);
     const float bias = p.bias ? p.bias[dc] : 0.f;
     const float Dd = p.D ? p.D[dc] : 0.f;
     const Tin *gu = static_cast<const Tin *>(p.u) + row * L;
@@ -359,15 +443,24 @@ __global__ void __launch_bounds__(32, 9) scan_bwd2_kernel(const ssh::BwdParams p
         const float2 v = *reinterpret_cast<const float2 *>(&sm.bc[t][N + 2 * j]);
         return mk2(v.x, v.y);
     };
+    // one forward step; du is dt * u (simplified) or u (zero-order hold)
     auto fwd_step = [&](f2 *h, float dt, float du, int t) {
         const float dl = dt * kLog2e;
         const f2 dd = mk2(dl, dl), uu = mk2(du, du);
 #pragma unroll
         for (int j = 0; j < NP; ++j) {
             const f2 tt = fmul2(dd, Ar[j]);
-            h[j] = ffma2(mk2(ex2(tt.x), ex2(tt.y)), h[j], fmul2(uu, Bpair(t, j)));
+            const f2 e = mk2(ex2(tt.x), ex2(tt.y));
+            if constexpr (ZH) {
+                const f2 dn = mk2(dt, dt);
+                const f2 f = zoh_f2(dn, fmul2(dn, Ar[j]), e, iA[j]);
+                h[j] = ffma2(e, h[j], fmul2(fmul2(f, uu), Bpair(t, j)));
+            } else {
+                h[j] = ffma2(e, h[j], fmul2(uu, Bpair(t, j)));
+            }
         }
     };
+    auto step_in = [&](float dt, float u) { return ZH ? u : dt * u; };
 
     // ---- forward sweep: the state entering every tile
     {
@@ -388,7 +481,7 @@ __global__ void __launch_bounds__(32, 9) scan_bwd2_kernel(const ssh::BwdParams p
             for (int t = 0; t < kTL; ++t) {
                 const float x = dl[t] + bias;
                 const float dt = p.softplus ? softplus1(x) : x;
-                fwd_step(h, dt, dt * uv[t], t);
+                fwd_step(h, dt, step_in(dt, uv[t]), t);
             }
         }
     }
@@ -442,7 +535,7 @@ __global__ void __launch_bounds__(32, 9) scan_bwd2_kernel(const ssh::BwdParams p
 #pragma unroll 1
                 for (int t = 0; t < kHalf; ++t) {
                     const float dtt = sm.io[0][t][lane];
-                    fwd_step(hp, dtt, dtt * sm.io[1][t][lane], t);
+                    fwd_step(hp, dtt, step_in(dtt, sm.io[1][t][lane]), t);
                 }
             }
             f2 hcur[NP];  // after the loop: the state after the half's last step
@@ -451,7 +544,7 @@ __global__ void __launch_bounds__(32, 9) scan_bwd2_kernel(const ssh::BwdParams p
 #pragma unroll 1
             for (int t = 0; t < kHalf; ++t) {
                 const float dtt = sm.io[0][t0 + t][lane];
-                fwd_step(hcur, dtt, dtt * sm.io[1][t0 + t][lane], t0 + t);
+                fwd_step(hcur, dtt, step_in(dtt, sm.io[1][t0 + t][lane]), t0 + t);
                 if (t < kHalf - 1) {
 #pragma unroll
                     for (int j = 0; j < NP; ++j) sm.S[t][j][lane] = make_float2(hcur[j].x, hcur[j].y);
@@ -492,14 +585,26 @@ __global__ void __launch_bounds__(32, 9) scan_bwd2_kernel(const ssh::BwdParams p
                     const f2 e = mk2(ex2(tq.x), ex2(tq.y));
                     g[j] = ffma2(gs2, Cp, g[j]);
                     const f2 vc = fmul2(gs2, hcur[j]);
-                    const f2 gdu = fmul2(g[j], dd);
-                    const f2 vb = fmul2(gdu, uu);
-                    v[2 * j] = vb.x, v[2 * j + 1] = vb.y;
                     v[N + 2 * j] = vc.x, v[N + 2 * j + 1] = vc.y;
-                    gu2 = ffma2(gdu, Bp, gu2);
                     const f2 ehp = fmul2(e, hprev[j]);
-                    gdt2 = ffma2(g[j], ffma2(Ar[j], ehp, fmul2(Bp, uu)), gdt2);
-                    gA[j] = ffma2(gdu, ehp, gA[j]);
+                    if constexpr (ZH) {
+                        f2 fa;
+                        const f2 f = zoh_factor2(dd, fmul2(dd, dd), fmul2(dd, Ar[j]), e, iA[j], &fa);
+                        const f2 gf = fmul2(g[j], f);
+                        const f2 vb = fmul2(gf, uu);
+                        v[2 * j] = vb.x, v[2 * j + 1] = vb.y;
+                        gu2 = ffma2(gf, Bp, gu2);
+                        const f2 bu = fmul2(Bp, uu);
+                        gdt2 = ffma2(g[j], ffma2(Ar[j], ehp, fmul2(e, bu)), gdt2);
+                        gA[j] = ffma2(g[j], ffma2(dd, ehp, fmul2(fa, bu)), gA[j]);
+                    } else {
+                        const f2 gdu = fmul2(g[j], dd);
+                        const f2 vb = fmul2(gdu, uu);
+                        v[2 * j] = vb.x, v[2 * j + 1] = vb.y;
+                        gu2 = ffma2(gdu, Bp, gu2);
+                        gdt2 = ffma2(g[j], ffma2(Ar[j], ehp, fmul2(Bp, uu)), gdt2);
+                        gA[j] = ffma2(gdu, ehp, gA[j]);
+                    }
                     g[j] = fmul2(g[j], e);
                     hcur[j] = hprev[j];
                 }
@@ -567,7 +672,8 @@ __global__ void __launch_bounds__(32, 9) scan_bwd2_kernel(const ssh::BwdParams p
     }
 }
 
-template <typename Tin, int N, typename Smem, typename Kern>
+// One instantiation (and so one attribute cache) per kernel: ZH is part of the key.
+template <typename Tin, int N, typename Smem, bool ZH, typename Kern>
 int bwd_launch(Kern kern, const ssh::BwdParams &p, cudaStream_t st) {
     const int smem = (int)sizeof(Smem);
     static bool attr_done[64] = {false};
@@ -586,10 +692,15 @@ int bwd_launch(Kern kern, const ssh::BwdParams &p, cudaStream_t st) {
 
 template <typename Tin, int N>
 int bwd_n(const ssh::BwdParams &p, cudaStream_t st) {
-    if constexpr (SS_BWD_PACKED && N % 2 == 0)
-        return bwd_launch<Tin, N, BwdSmem2<N>>(scan_bwd2_kernel<Tin, N>, p, st);
-    else
-        return bwd_launch<Tin, N, BwdSmem<N>>(scan_bwd_kernel<Tin, N>, p, st);
+    if constexpr (SS_BWD_PACKED && N % 2 == 0) {
+        if (p.zoh)
+            return bwd_launch<Tin, N, BwdSmem2<N>, true>(scan_bwd2_kernel<Tin, N, true>, p, st);
+        return bwd_launch<Tin, N, BwdSmem2<N>, false>(scan_bwd2_kernel<Tin, N, false>, p, st);
+    } else {
+        if (p.zoh)
+            return bwd_launch<Tin, N, BwdSmem<N>, true>(scan_bwd_kernel<Tin, N, true>, p, st);
+        return bwd_launch<Tin, N, BwdSmem<N>, false>(scan_bwd_kernel<Tin, N, false>, p, st);
+    }
 }
 
 template <typename Tin>

@@ -120,6 +120,7 @@ struct BwdParams {
     const float *dy, *dh_last;
     float *du, *ddelta, *dz, *dA, *dB, *dC, *dD, *dbias, *dh0;
     float *ckpt;  // scratch: bwd_ckpt_bytes
+    int zoh;      // exact zero-order-hold input matrix (the scalar backward kernel)
 };
 size_t bwd_ckpt_bytes(const BwdParams &p);
 bool bwd_supported(const BwdParams &p);
