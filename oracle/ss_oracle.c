@@ -354,6 +354,8 @@ int ss_oracle_scan_bwd(long long nrows, const int *row_b, const int *row_d, int 
                 if (zoh && a != 0.0) {
                     fdt = e;                                  /* d/ddt (e^{dt a}-1)/a */
                     fa = (dt * e) / a - expm1(dt * a) / (a * a);
+                } else if (zoh) {
+                    fa = 0.5 * dt * dt;                       /* its limit at a = 0 */
                 }
                 if (dB) dB[bcrow + (long long)n * L + t] += g[n] * f * uv;
                 gu += g[n] * f * Bv;

@@ -349,7 +349,7 @@ def pin_zoh_decode_chain(orc, seed=32, k=10):
 # perturbed one element at a time. fp32 inputs move by a power of two so the
 # perturbed values are exact; the forward runs in fp64.
 
-def _fd_case(seed, zoh=False, softplus=True):
+def _fd_case(seed, zoh=False, softplus=True, a_zero=False):
     g = np.random.default_rng(seed)
     batch, dim, N, L = 2, 2, 3, 6
     f = lambda *s: g.standard_normal(s).astype(np.float32)
@@ -357,6 +357,8 @@ def _fd_case(seed, zoh=False, softplus=True):
              A=-(g.uniform(0.3, 2.0, (dim, N))).astype(np.float32), B=f(batch, N, L),
              C=f(batch, N, L), D=f(dim), delta_bias=(g.uniform(-2.0, 0.5, dim)).astype(np.float32),
              h0=g.standard_normal((batch, dim, N)))
+    if a_zero:  # state 0 of every channel without decay: the ZOH factor's a = 0 limit
+        c["A"][:, 0] = 0.0
     if not softplus:
         c["delta"] = (np.abs(c["delta"]) * 0.3).astype(np.float32)
         c["delta_bias"] = (np.abs(c["delta_bias"]) * 0.1).astype(np.float32)
@@ -372,8 +374,8 @@ def _loss(orc, c, dy, dh, zoh, softplus):
     return float(np.sum(dy * y) + np.sum(dh * hl))
 
 
-def pin_bwd_finite_diff(orc, seed=40, zoh=False, softplus=True):
-    c, dy, dh = _fd_case(seed, zoh, softplus)
+def pin_bwd_finite_diff(orc, seed=40, zoh=False, softplus=True, a_zero=False):
+    c, dy, dh = _fd_case(seed, zoh, softplus, a_zero)
     grads = orc.scan_bwd(c["u"], c["delta"], c["A"], c["B"], c["C"], dy, D=c["D"],
                          delta_bias=c["delta_bias"], z=c["z"], delta_softplus=softplus, h0=c["h0"],
                          dh_last=dh, zoh=zoh)
@@ -530,6 +532,7 @@ ALL_PINS = {
     "zoh_decode_chain": pin_zoh_decode_chain,
     "bwd_finite_diff": pin_bwd_finite_diff,
     "bwd_finite_diff_zoh": lambda o: pin_bwd_finite_diff(o, seed=41, zoh=True),
+    "bwd_finite_diff_zoh_a0": lambda o: pin_bwd_finite_diff(o, seed=43, zoh=True, a_zero=True),
     "bwd_finite_diff_no_softplus": lambda o: pin_bwd_finite_diff(o, seed=42, softplus=False),
     "conv_numpy": pin_conv_numpy,
     "conv_impulse": pin_conv_impulse,
@@ -541,5 +544,6 @@ ALL_PINS = {
 
 # every pin must come in under this (fp64 everywhere)
 PIN_TOL = {"small_delta": 1e-9, "bwd_finite_diff": 1e-6, "bwd_finite_diff_zoh": 1e-6,
+           "bwd_finite_diff_zoh_a0": 1e-6,
            "bwd_finite_diff_no_softplus": 1e-6}
 DEFAULT_TOL = 1e-11

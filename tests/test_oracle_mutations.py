@@ -49,6 +49,7 @@ MUTANTS = {
                               "gdt += g[n] * (a * e * hp);"),
     "bwd_dz_sigmoid_only": ("dy[urow + t] * s * sg * (1.0 + zv * (1.0 - sg))", "dy[urow + t] * s * sg"),
     "bwd_zoh_fa_dropped": ("(dt * e * hp + fa * Bv * uv)", "(dt * e * hp)"),
+    "bwd_zoh_fa_limit_dropped": ("fa = 0.5 * dt * dt;", "fa = 0.0;"),
     "bwd_gx_no_sigmoid": ("const double gx = delta_softplus ? gdt / (1.0 + exp(-x)) : gdt;",
                           "const double gx = gdt;"),
     "bwd_dh_last_ignored": ("g[n] = dh_last ? dh_last[r * N + n] : 0.0;", "g[n] = 0.0;"),
