@@ -20,14 +20,23 @@
 // One CTA of 8 warps per (batch, head). Warp w reads TMEM lanes
 // [32 (w % 4), 32 (w % 4) + 32) (rows t of G, Y, Z; rows n of S) and takes half
 // w / 4 of each epilogue's columns. Thread 0 issues the MMAs and commits them
-// to one mbarrier; the other threads meanwhile build Xs and rescale S. C and B
-// are double-buffered and the next chunk's x and dt wait in registers, so a
-// chunk's loads overlap the previous chunk's work. Shared
+// to one mbarrier; the other threads meanwhile build Xs and rescale S, and
+// warp 0 forms the next chunk's dt and its prefix sum while the Y, Z and S
+// products run. C and B are double-buffered and the next chunk's x and dt wait
+// in registers, so a chunk's loads overlap the previous chunk's work. y leaves
+// through a 128-byte-swizzled shared tile (the masked tile's buffer, free once
+// Y is done) by TMA stores, whole rows at a time. The mask's exponentials
+// below the diagonal 32 x 32 band are factored per 16-column block with end e:
+// exp2(cum_t - cum_s) = exp2(cum_t - cum_e) exp2(cum_e - cum_s), both factors
+// at most 1 (cum falls along the chunk), one exponential per row and block
+// plus one per column, instead of one per element. Shared
 // operand tiles are stored as 8-row x 16-byte core matrices, column blocks
 // fastest, and described to the tensor core without swizzling: K-major tiles
 // (C, B, M) with the leading offset between K-adjacent core matrices and the
 // stride offset between 8-row groups; MN-major tiles (X, Xs, H, and B read as
 // B^T) the other way round.
+#include <cudaTypedefs.h>
+
 #include "ss_common.cuh"
 #include "ss_internal.h"
 
@@ -53,6 +62,7 @@ struct TcSmem {
                               // MN-major B of one 128-column Z product
     float dt[kQ];
     float cum[kQ];
+    float W[kQ];  // exp2(cum_e - cum_s) dt_s, e the last step of s's 16-column block
     uint64_t bar;
     uint32_t tmem;
 };
@@ -86,6 +96,10 @@ constexpr uint32_t kKmLbo = 128, kKmSbo = 128 * (kQ / 8);  // K-major 128-column
 constexpr uint32_t kKmStep = 256;                          // 16 columns of K
 constexpr uint32_t kMn64Lbo = 128 * (kP / 8), kMn64Sbo = 128, kMn64Step = 2 * kMn64Lbo;
 constexpr uint32_t kMn128Lbo = 128 * (kN / 8), kMn128Sbo = 128, kMn128Step = 2 * kMn128Lbo;
+
+// A descriptor advanced by `bytes` along its start address (no carry out of
+// the 14-bit field: every tile lies within the first 256 KB of shared memory).
+__device__ __forceinline__ uint64_t dadv(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t id,
                                         bool accumulate) {
@@ -177,6 +191,30 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 2D TMA store shared -> global of one box (bulk group of the issuing thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, int x, int y, const void *src) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(tm)),
+        "r"(x), "r"(y), "r"(smem_u32(src))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the shared-memory sources of every committed store have been read
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Byte offset of 16-byte piece j of row r in a tile of 128-byte rows stored
+// with the 128-byte swizzle (piece index XOR row mod 8).
+__device__ __forceinline__ uint32_t sw128(int r, int j) {
+    return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4));
+}
+
 // Global loads kept in program order (volatile): issued where written, one
 // chunk ahead of their use, rather than moved next to it.
 __device__ __forceinline__ uint4 ldg_v4_ordered(const void *p) {
@@ -225,27 +263,36 @@ __device__ __forceinline__ bool mma_wait(uint64_t *bar, uint32_t parity, uint32_
     return false;
 }
 
-__device__ __forceinline__ void store16(float *dst, const float (&v)[16]) {
+// 16 y values of row t, channels c .. c + 15 of the head, into the staging
+// tile: fp32 output as two boxes of 32 channels (16 KB each), bf16 as one box
+// of 64 channels; 128-byte rows, swizzled.
+__device__ __forceinline__ void stage16(uint8_t *st, int t, int c, const float (&v)[16], float) {
+    uint8_t *box = st + (c >> 5) * (kQ * 128);
+    const int j0 = (c & 31) >> 2;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        reinterpret_cast<float4 *>(dst)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        *reinterpret_cast<float4 *>(box + sw128(t, j0 + j)) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
 }
-__device__ __forceinline__ void store16(uint16_t *dst, const float (&v)[16]) {
+__device__ __forceinline__ void stage16(uint8_t *st, int t, int c, const float (&v)[16], uint16_t) {
     uint32_t w[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) w[j] = pack2(v[2 * j], v[2 * j + 1]);
-    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    const int j0 = c >> 3;
+    *reinterpret_cast<uint4 *>(st + sw128(t, j0)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4 *>(st + sw128(t, j0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 constexpr int kThreads = 256;  // 8 warps: warp w serves TMEM lanes 32 (w % 4) .. +32 and
                                // column half w / 4 of each epilogue
 
 template <typename Tout>
-__global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_tc_kernel(const __grid_constant__ CUtensorMap tm_y, const ssh::SsdParams p) {
     extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned: the y staging tile (in M) is read with the 128-byte swizzle
     TcSmem &sm = *reinterpret_cast<TcSmem *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sM = reinterpret_cast<uint8_t *>(sm.M), *sX = reinterpret_cast<uint8_t *>(sm.X);
     uint8_t *sXs = reinterpret_cast<uint8_t *>(sm.Xs);
     uint8_t *sH = reinterpret_cast<uint8_t *>(sm.H);
@@ -266,14 +313,29 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
     const long long st_base = ((long long)b * p.heads + h) * kP * kN;  // h0 / h_last (p, n)
     const int n_chunks = (int)(L / kQ);
 
-    // C and B of chunk c into buffer c & 1 (16-byte asynchronous copies, one group)
-    auto issue_cb = [&](int c) {
+    // The 16-byte pieces of a tile moved by one warp instruction: 8 rows (lane
+    // mod 8) by 4 adjacent pieces (lane / 8), so the global side reads 8 rows x
+    // 64 contiguous bytes (16 whole sectors) and each group of 8 lanes writes 8
+    // rows of one core matrix (distinct banks). Block k of warp w is block
+    // w + 8 k of the tile's (rows / 8) x (pieces / 4) blocks, pieces fastest.
+    auto piece = [&](int k, int blocks_per_row_group, int &row, int &pc) {
+        const int blk = warp + 8 * k;
+        row = 8 * (blk / blocks_per_row_group) + (lane & 7);
+        pc = 4 * (blk % blocks_per_row_group) + (lane >> 3);
+    };
+    // Quarter q of C and B of chunk c into buffer c & 1 (16-byte asynchronous
+    // copies, one group per quarter). The quarters of the next chunk are issued
+    // at four points of this chunk: a thread can have only so many copies in
+    // flight, and issuing all 16 at once held every thread ~4K cycles.
+    constexpr int kCbPieces = kQ * kN / 8 / kThreads;  // per thread and tensor
+    auto issue_cb = [&](int c, int q) {
         uint8_t *dC = reinterpret_cast<uint8_t *>(sm.C[c & 1]);
         uint8_t *dB = reinterpret_cast<uint8_t *>(sm.B[c & 1]);
         const long long l0 = (long long)c * kQ;
 #pragma unroll
-        for (int k = 0; k < kQ * kN / 8 / kThreads; ++k) {
-            const int i = tid + kThreads * k, t = i % kQ, n8 = i / kQ;
+        for (int k = q * kCbPieces / 4; k < (q + 1) * kCbPieces / 4; ++k) {
+            int t, n8;
+            piece(k, kN / 32, t, n8);
             const long long g = ((long long)b * L + l0 + t) * kN + 8 * n8;
             cp_async16(dC + cm_off(t, 8 * n8, kN), gC + g, 16);
             cp_async16(dB + cm_off(t, 8 * n8, kN), gB + g, 16);
@@ -286,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         const long long l0 = (long long)c * kQ;
 #pragma unroll
         for (int k = 0; k < kXPieces; ++k) {
-            const int i = tid + kThreads * k, s = i % kQ, p8 = i / kQ;
+            int s, p8;
+            piece(k, kP / 32, s, p8);
             xr[k] = ldg_v4_ordered(gx + ((long long)b * L + l0 + s) * xs_t + (long long)h * kP + 8 * p8);
         }
     };
@@ -296,6 +359,37 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             dr[k] = ldg_u16_ordered(gdt + ((long long)b * L + l0 + 4 * lane + k) * p.heads + h);
+    };
+
+    // dt, its running sum (times a, log2 units) and the block weights W of a
+    // chunk from raw dt, four steps per lane of warp 0, into registers
+    auto dt_scan = [&](const uint16_t (&raw)[4], float (&d4)[4], float (&c4)[4], float (&w4)[4]) {
+        float run = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float xv = to_f32(raw[k]) + bias;
+            d4[k] = p.softplus ? softplus1(xv) : xv;
+            run += d4[k] * a;
+            c4[k] = run;
+        }
+        float incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        const float before = incl - run;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c4[k] += before;
+        // the block of 16 steps is 4 lanes; its last step is lane | 3's fourth
+        const float ce = __shfl_sync(0xffffffffu, c4[3], lane | 3);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w4[k] = ex2(ce - c4[k]) * d4[k];
+    };
+    auto dt_put = [&](const float (&d4)[4], const float (&c4)[4], const float (&w4)[4]) {
+        *reinterpret_cast<float4 *>(&sm.dt[4 * lane]) = make_float4(d4[0], d4[1], d4[2], d4[3]);
+        *reinterpret_cast<float4 *>(&sm.cum[4 * lane]) = make_float4(c4[0], c4[1], c4[2], c4[3]);
+        *reinterpret_cast<float4 *>(&sm.W[4 * lane]) = make_float4(w4[0], w4[1], w4[2], w4[3]);
     };
 
     if (warp == 0) {
@@ -310,19 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         mbar_init(&sm.bar, 1);
         fence_mbar_init();
     }
-    // The masked tile's 16-byte pieces right of a 32-row band are zero in every
-    // chunk (s > t there): written once.
-    for (int i = tid; i < kQ * kQ / 8; i += kThreads) {
-        const int t = i % kQ, s8 = i / kQ;
-        if (8 * s8 >= 32 * (t / 32 + 1))
-            *reinterpret_cast<uint4 *>(sM + cm_off(t, 8 * s8, kQ)) = make_uint4(0u, 0u, 0u, 0u);
-    }
     uint4 xr[kXPieces];
     uint16_t dr[4] = {0, 0, 0, 0};
+    float nd[4] = {0.f, 0.f, 0.f, 0.f}, nc[4] = {0.f, 0.f, 0.f, 0.f}, nw[4] = {0.f, 0.f, 0.f, 0.f};
     if (n_chunks > 0) {
-        issue_cb(0);
+        for (int q = 0; q < 4; ++q) issue_cb(0, q);
         load_x(0, xr);
-        if (warp == 0) load_dt(0, dr);
+        if (warp == 0) {
+            load_dt(0, dr);
+            dt_scan(dr, nd, nc, nw);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -353,34 +444,15 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         // ---- x of the chunk from registers into its tile; dt and its prefix sum
 #pragma unroll
         for (int k = 0; k < kXPieces; ++k) {
-            const int i = tid + kThreads * k, s = i % kQ, p8 = i / kQ;
+            int s, p8;
+            piece(k, kP / 32, s, p8);
             *reinterpret_cast<uint4 *>(sX + cm_off(s, 8 * p8, kP)) = xr[k];
         }
-        if (warp == 0) {
-            float d4[4], c4[4], run = 0.f;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float xv = to_f32(dr[k]) + bias;
-                d4[k] = p.softplus ? softplus1(xv) : xv;
-                run += d4[k] * a;
-                c4[k] = run;
-            }
-            float incl = run;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += o;
-            }
-            const float before = incl - run;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                sm.dt[4 * lane + k] = d4[k];
-                sm.cum[4 * lane + k] = before + c4[k];
-            }
-        }
+        if (warp == 0) dt_put(nd, nc, nw);  // formed during the previous chunk
         // ---- the next chunk's operands start moving now
-        if (c + 1 < n_chunks) {
-            issue_cb(c + 1);
+        const bool more = c + 1 < n_chunks;
+        if (more) {
+            issue_cb(c + 1, 0);
             load_x(c + 1, xr);
             if (warp == 0) load_dt(c + 1, dr);
             cp_async_wait<1>();  // this chunk's C and B have landed
@@ -394,12 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
 
         // ---- G = C B^T into TMEM columns [0, 128)
         if (tid == 0) {
+            const uint64_t dC = sdesc(sC, 0, kKmLbo, kKmSbo), dB = sdesc(sB, 0, kKmLbo, kKmSbo);
 #pragma unroll
             for (int k = 0; k < kN / 16; ++k)
-                mma_f16(tmem + kColG, sdesc(sC, k * kKmStep, kKmLbo, kKmSbo),
-                        sdesc(sB, k * kKmStep, kKmLbo, kKmSbo), kIdG, k > 0);
+                mma_f16(tmem + kColG, dadv(dC, k * kKmStep), dadv(dB, k * kKmStep), kIdG, k > 0);
             mma_commit(&sm.bar);
         }
+        if (more) issue_cb(c + 1, 1);
         const float cum_last = sm.cum[kQ - 1];
         // ---- meanwhile: Xs (row s = r, this half's 4 pieces) and S scaled by
         // the chunk's decay in place (row r, this half's 32 columns)
@@ -425,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
             tmem_st16(trow + kColS + c0 + 16, v1);
             tmem_wait_st();
         }
+        if (tid == 0) bulk_wait_read();  // the previous chunk's y has left the M buffer
         if (__syncthreads_or(!mma_wait(&sm.bar, phase, p.wait_limit))) {
             if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
             timed_out = true;
@@ -439,20 +513,35 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
             const int t = r;
             const float ct = sm.cum[t];
             // this warp's pieces j = half, half + 2, ... (quarter + 1 of them), two per load
+            // pieces left of the band (s0 + 16 <= 32 quarter <= t for every lane of
+            // the warp) take the factored form; the band's two pieces the direct one
             auto mask_piece = [&](int s0, const float (&g)[16]) {
                 uint32_t w[8];
+                if (s0 + 16 <= 32 * quarter) {
+                    const float E = ex2(ct - sm.cum[s0 + 15]);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int s = s0 + 2 * i;
-                    const float m0 = s <= t ? g[2 * i] * ex2(ct - sm.cum[s]) * sm.dt[s] : 0.f;
-                    const float m1 =
-                        s + 1 <= t ? g[2 * i + 1] * ex2(ct - sm.cum[s + 1]) * sm.dt[s + 1] : 0.f;
-                    w[i] = pack2(m0, m1);
+                    for (int i = 0; i < 8; ++i) {
+                        const int s = s0 + 2 * i;
+                        w[i] = pack2(g[2 * i] * E * sm.W[s], g[2 * i + 1] * E * sm.W[s + 1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int s = s0 + 2 * i;
+                        const float m0 = s <= t ? g[2 * i] * ex2(ct - sm.cum[s]) * sm.dt[s] : 0.f;
+                        const float m1 = s + 1 <= t
+                                             ? g[2 * i + 1] * ex2(ct - sm.cum[s + 1]) * sm.dt[s + 1]
+                                             : 0.f;
+                        w[i] = pack2(m0, m1);
+                    }
                 }
                 *reinterpret_cast<uint4 *>(sM + cm_off(t, s0, kQ)) = make_uint4(w[0], w[1], w[2], w[3]);
                 *reinterpret_cast<uint4 *>(sM + cm_off(t, s0 + 8, kQ)) =
                     make_uint4(w[4], w[5], w[6], w[7]);
             };
+            // right of the band s > t: zeros (the buffer held the last chunk's y)
+            for (int s8 = 4 * (quarter + 1) + half; s8 < kQ / 8; s8 += 2)
+                *reinterpret_cast<uint4 *>(sM + cm_off(t, 8 * s8, kQ)) = make_uint4(0u, 0u, 0u, 0u);
             for (int k = 0; k <= quarter; k += 2) {
                 const int s0 = 16 * (half + 2 * k);
                 if (k + 1 <= quarter) {
@@ -467,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
                 }
             }
         }
+        if (more) issue_cb(c + 1, 2);
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
@@ -474,20 +564,25 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
 
         // ---- Y = M X, Z = C [H_hi | H_lo] (into G's columns), S += B^T Xs
         if (tid == 0) {
+            const uint64_t dM = sdesc(sM, 0, kKmLbo, kKmSbo), dX = sdesc(sX, 0, kMn64Lbo, kMn64Sbo);
+            const uint64_t dC = sdesc(sC, 0, kKmLbo, kKmSbo), dH = sdesc(sH, 0, kMn128Lbo, kMn128Sbo);
+            const uint64_t dBt = sdesc(sB, 0, kMn128Lbo, kMn128Sbo);
+            const uint64_t dXs = sdesc(sXs, 0, kMn64Lbo, kMn64Sbo);
 #pragma unroll
             for (int k = 0; k < kQ / 16; ++k)
-                mma_f16(tmem + kColY, sdesc(sM, k * kKmStep, kKmLbo, kKmSbo),
-                        sdesc(sX, k * kMn64Step, kMn64Lbo, kMn64Sbo), kIdY, k > 0);
+                mma_f16(tmem + kColY, dadv(dM, k * kKmStep), dadv(dX, k * kMn64Step), kIdY, k > 0);
 #pragma unroll
             for (int k = 0; k < kN / 16; ++k)
-                mma_f16(tmem + kColG, sdesc(sC, k * kKmStep, kKmLbo, kKmSbo),
-                        sdesc(sH, k * kMn128Step, kMn128Lbo, kMn128Sbo), kIdZ, k > 0);
+                mma_f16(tmem + kColG, dadv(dC, k * kKmStep), dadv(dH, k * kMn128Step), kIdZ, k > 0);
 #pragma unroll
             for (int k = 0; k < kQ / 16; ++k)
-                mma_f16(tmem + kColS, sdesc(sB, k * kMn128Step, kMn128Lbo, kMn128Sbo),
-                        sdesc(sXs, k * kMn64Step, kMn64Lbo, kMn64Sbo), kIdS, true);
+                mma_f16(tmem + kColS, dadv(dBt, k * kMn128Step), dadv(dXs, k * kMn64Step), kIdS, true);
             mma_commit(&sm.bar);
         }
+        // meanwhile: the next chunk's dt, running sum and block weights (its raw
+        // dt was loaded at this chunk's start)
+        if (more) issue_cb(c + 1, 3);
+        if (warp == 0 && more) dt_scan(dr, nd, nc, nw);
         if (__syncthreads_or(!mma_wait(&sm.bar, phase, p.wait_limit))) {
             if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
             timed_out = true;
@@ -496,13 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
         phase ^= 1u;
         tc_fence_after();
 
-        // ---- y row t = r, this half's 32 channels; the new state's row n = r
-        // (same columns) into H
+        // ---- y row t = r, this half's 32 channels, into the staging tile (the M
+        // buffer) and out by TMA; the new state's row n = r (same columns) into H
         {
             const int t = r;
             const float ft = ex2(sm.cum[t]);
-            Tout *dst = static_cast<Tout *>(p.y) + ((long long)b * L + l0 + t) * xs_t +
-                        (long long)h * kP + c0;
             float y0[16], y1[16], zh0[16], zh1[16], zl0[16], zl1[16];
             tmem_ld16x4(trow + kColY + c0, trow + kColY + c0 + 16, trow + kColG + c0,
                         trow + kColG + c0 + 16, y0, y1, zh0, zh1);
@@ -517,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
                     yv[2 * i + 1] = fmaf(Dh, bf16hi(xw[i]),
                                          fmaf(ft, zh[2 * i + 1] + zl[2 * i + 1], yv[2 * i + 1]));
                 }
-                store16(dst + 16 * j, yv);
+                stage16(sM, t, c0 + 16 * j, yv, Tout());
             };
             finish(0, y0, zh0, zl0);
             finish(1, y1, zh1, zl1);
@@ -526,7 +619,20 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
             put_state16(sH, t, c0, v0);
             put_state16(sH, t, c0 + 16, v1);
         }
+        fence_proxy_async();  // the staged y is visible to the TMA unit
+        __syncthreads();
+        if (tid == 0) {
+            const int yrow = (int)((long long)b * L + l0);
+            if (sizeof(Tout) == 4) {
+                tma_store_2d(&tm_y, h * kP, yrow, sM);
+                tma_store_2d(&tm_y, h * kP + 32, yrow, sM + kQ * 128);
+            } else {
+                tma_store_2d(&tm_y, h * kP, yrow, sM);
+            }
+            bulk_commit();
+        }
     }
+    if (tid == 0) bulk_wait_all();  // the y stores have completed
     cp_async_wait<0>();  // nothing left in flight if a wait gave up
     // after a wait that gave up, give the committed products one more bounded
     // wait before their tensor memory is freed
@@ -551,10 +657,37 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const ssh::SsdParam
     }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
 template <typename Tout>
 int ssd_tc_t(const ssh::SsdParams &p, cudaStream_t st) {
-    const int smem = (int)sizeof(TcSmem) + 128;
+    const int smem = (int)sizeof(TcSmem) + 1024;
     auto kern = ssd_tc_kernel<Tout>;
+    // y as rows of heads * 64 channels, one row per (batch, step); boxes of 128
+    // rows by 128 bytes (32 fp32 or 64 bf16 channels), 128-byte swizzle
+    auto fn = encode_fn();
+    if (!fn) return SS_ERR_UNSUPPORTED;
+    CUtensorMap tm;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.heads * kP, (cuuint64_t)p.batch * p.seqlen};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.heads * kP * sizeof(Tout)};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / sizeof(Tout)), (cuuint32_t)kQ};
+    const cuuint32_t estr[2] = {1, 1};
+    if (fn(&tm, sizeof(Tout) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+           2, p.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SS_ERR_UNSUPPORTED;
     static bool done[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
@@ -564,15 +697,18 @@ int ssd_tc_t(const ssh::SsdParams &p, cudaStream_t st) {
             return SS_ERR_CUDA;
         done[dev] = true;
     }
-    kern<<<(unsigned)((long long)p.batch * p.heads), kThreads, smem, st>>>(p);
+    kern<<<(unsigned)((long long)p.batch * p.heads), kThreads, smem, st>>>(tm, p);
     return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 }  // namespace
 
 bool ssh::ssd_tc_supported(const ssh::SsdParams &p) {
+    // y leaves by TMA: a 16-byte aligned base and (batch, step) rows indexable in 32 bits
     return p.in_dtype == SS_BF16 && p.headdim == kP && p.dstate == kN && p.seqlen % kQ == 0 &&
-           (long long)p.batch * p.heads < (1LL << 31);
+           (long long)p.batch * p.heads < (1LL << 31) &&
+           (long long)p.batch * p.seqlen < (1LL << 31) &&
+           (reinterpret_cast<uintptr_t>(p.y) & 15u) == 0 && encode_fn() != nullptr;
 }
 
 int ssh::launch_ssd_tc(const ssh::SsdParams &p, cudaStream_t st) {
