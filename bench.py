@@ -540,11 +540,11 @@ def time_ssd(ss, ctx, dev, stream, args, batch=8, L=2048, H=80, P=64, N=128, pro
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) * 1e3 / steps
 
-    # the tensor-memory (tcgen05) kernel on the same call, for comparison
-    tc_ctx = ss.Context(dev.index if dev.index is not None else 0)
-    tc_ctx.set_option(ss.SS_OPT_SSD_PATH, ss.SS_SSD_PATH_TCGEN05)
-    us_tc = timed(tc_ctx.handle)
-    tc_ctx.close()
+    # the warp-level mma.sync kernel on the same call, for comparison
+    mma_ctx = ss.Context(dev.index if dev.index is not None else 0)
+    mma_ctx.set_option(ss.SS_OPT_SSD_PATH, ss.SS_SSD_PATH_MMA_SYNC)
+    us_mma = timed(mma_ctx.handle)
+    mma_ctx.close()
     us = timed(ctx.handle)
     path = "tensor memory (tcgen05)" if ctx.last_launch()[0] == 1 else "mma.sync"
     Q = 64
@@ -562,7 +562,7 @@ def time_ssd(ss, ctx, dev, stream, args, batch=8, L=2048, H=80, P=64, N=128, pro
     hbm, src = measured_peaks()
     legacy = None
     m = (probes or {}).get("mma_sync_bf16")
-    if m and m.get("rc") == 0 and m.get("sm_ghz", 0) > 0:
+    if path == "mma.sync" and m and m.get("rc") == 0 and m.get("sm_ghz", 0) > 0:
         # what mma.sync (the tensor-core path this kernel uses) sustains, at the maximum clock
         lp = m["ops_per_s"] * (MAX_SM_MHZ * 1e-3) / m["sm_ghz"] / 1e12
         legacy = {"peak_tflops": lp, "frac": tflops / lp,
@@ -570,7 +570,7 @@ def time_ssd(ss, ctx, dev, stream, args, batch=8, L=2048, H=80, P=64, N=128, pro
     return {"workload": "ssd (Mamba-2): batch %d, L %d, %d heads x %d, d_state %d, bf16 in, "
                         "fp32 y" % (batch, L, H, P, N),
             "flops_counted_at_chunk": Q,
-            "kernel": path, "us_per_call": us, "tcgen05_kernel_us_per_call": us_tc,
+            "kernel": path, "us_per_call": us, "mma_sync_kernel_us_per_call": us_mma,
             "elements_per_s": batch * L * H * P / (us * 1e-6),
             "tensor": {"achieved_tflops": tflops, "peak_tflops": peak_t,
                        "frac": tflops / peak_t, "note": "algorithmic bf16 products (the state's "

@@ -396,14 +396,17 @@ const char *ss_status_string(int status);
  *                           of this tile index, so its wait runs out and the
  *                           timeout path is exercised (-1 = off, the default).
  *   SS_OPT_SSD_PATH         tensor-core kernel of ss_ssd_fwd:
- *                           SS_SSD_PATH_AUTO (default) and SS_SSD_PATH_MMA_SYNC
- *                           run the warp-level mma.sync kernel (64-step
- *                           chunks), the faster of the two at the Mamba-2
- *                           block shape; SS_SSD_PATH_TCGEN05 runs the
- *                           tensor-memory kernel (tcgen05 products with
- *                           accumulators in tensor memory, 128-step chunks;
- *                           headdim 64, dstate 128, seqlen a multiple of 128,
- *                           else SS_ERR_UNSUPPORTED).
+ *                           SS_SSD_PATH_TCGEN05 runs the tensor-memory kernel
+ *                           (tcgen05 products with accumulators in tensor
+ *                           memory, 128-step chunks, operands and y moved by
+ *                           TMA; headdim 64, dstate 128, seqlen a multiple of
+ *                           128, y, B and C 16-byte aligned, else
+ *                           SS_ERR_UNSUPPORTED); SS_SSD_PATH_MMA_SYNC runs the
+ *                           warp-level mma.sync kernel (64-step chunks, any
+ *                           headdim multiple of 16 and dstate 64 or 128);
+ *                           SS_SSD_PATH_AUTO (default) takes the tensor-memory
+ *                           kernel wherever it applies (the faster of the two
+ *                           at the Mamba-2 block shape), else mma.sync.
  * Returns SS_OK or SS_ERR_INVALID_ARG (unknown option or value out of range).
  */
 typedef enum {

@@ -559,7 +559,10 @@ int ss_ssd_fwd(ss_ctx *ctx, const ss_ssd_args *a, ss_stream_t stream) {
     ssh::SsdParams p{a->batch, a->heads, a->headdim, a->dstate, a->seqlen, a->in_dtype,
                      a->out_dtype, a->x, a->dt, a->A, a->B, a->C, a->D, a->dt_bias,
                      a->dt_softplus, a->h0, a->y, a->h_last, ctx->d_err, ctx->wait_limit};
-    const bool tc = ctx->ssd_path == SS_SSD_PATH_TCGEN05;
+    // AUTO takes the tensor-memory kernel wherever it applies (the faster one),
+    // else the mma.sync kernel
+    const bool tc = ctx->ssd_path == SS_SSD_PATH_TCGEN05 ||
+                    (ctx->ssd_path == SS_SSD_PATH_AUTO && ssh::ssd_tc_supported(p));
     if (tc ? !ssh::ssd_tc_supported(p) : !ssh::ssd_supported(p)) return SS_ERR_UNSUPPORTED;
     if (set_device(ctx) != SS_OK) return SS_ERR_CUDA;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

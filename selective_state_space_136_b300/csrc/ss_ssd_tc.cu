@@ -64,6 +64,7 @@ struct TcSmem {
     float cum[kQ];
     float W[kQ];  // exp2(cum_e - cum_s) dt_s, e the last step of s's 16-column block
     uint64_t bar;
+    uint64_t cbar[2];  // TMA arrival of C and B into buffer 0 / 1
     uint32_t tmem;
 };
 
@@ -191,6 +192,17 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 4D tiled TMA load global -> shared, completion signalled on `bar`.
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, int c0, int c1,
+                                            int c2, int c3, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
 // 2D TMA store shared -> global of one box (bulk group of the issuing thread).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, int x, int y, const void *src) {
     asm volatile(
@@ -288,7 +300,8 @@ constexpr int kThreads = 256;  // 8 warps: warp w serves TMEM lanes 32 (w % 4) .
 
 template <typename Tout>
 __global__ void __launch_bounds__(kThreads, 1)
-    ssd_tc_kernel(const __grid_constant__ CUtensorMap tm_y, const ssh::SsdParams p) {
+    ssd_tc_kernel(const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_c,
+                  const __grid_constant__ CUtensorMap tm_b, const ssh::SsdParams p) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned: the y staging tile (in M) is read with the 128-byte swizzle
     TcSmem &sm = *reinterpret_cast<TcSmem *>(
@@ -307,8 +320,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float Dh = p.D ? p.D[h] : 0.f;
     const long long xs_t = (long long)p.heads * kP;  // x / y stride between steps
     const uint16_t *gx = static_cast<const uint16_t *>(p.x);
-    const uint16_t *gB = static_cast<const uint16_t *>(p.B);
-    const uint16_t *gC = static_cast<const uint16_t *>(p.C);
     const uint16_t *gdt = static_cast<const uint16_t *>(p.dt);
     const long long st_base = ((long long)b * p.heads + h) * kP * kN;  // h0 / h_last (p, n)
     const int n_chunks = (int)(L / kQ);
@@ -323,24 +334,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         row = 8 * (blk / blocks_per_row_group) + (lane & 7);
         pc = 4 * (blk % blocks_per_row_group) + (lane >> 3);
     };
-    // Quarter q of C and B of chunk c into buffer c & 1 (16-byte asynchronous
-    // copies, one group per quarter). The quarters of the next chunk are issued
-    // at four points of this chunk: a thread can have only so many copies in
-    // flight, and issuing all 16 at once held every thread ~4K cycles.
-    constexpr int kCbPieces = kQ * kN / 8 / kThreads;  // per thread and tensor
-    auto issue_cb = [&](int c, int q) {
-        uint8_t *dC = reinterpret_cast<uint8_t *>(sm.C[c & 1]);
-        uint8_t *dB = reinterpret_cast<uint8_t *>(sm.B[c & 1]);
-        const long long l0 = (long long)c * kQ;
-#pragma unroll
-        for (int k = q * kCbPieces / 4; k < (q + 1) * kCbPieces / 4; ++k) {
-            int t, n8;
-            piece(k, kN / 32, t, n8);
-            const long long g = ((long long)b * L + l0 + t) * kN + 8 * n8;
-            cp_async16(dC + cm_off(t, 8 * n8, kN), gC + g, 16);
-            cp_async16(dB + cm_off(t, 8 * n8, kN), gB + g, 16);
-        }
-        cp_async_commit();
+    // C and B of chunk c into buffer c & 1 by TMA (thread 0): each tile is a 4D
+    // box (n mod 8, t mod 8, n / 8, t / 8) whose shared-memory image is the
+    // core-matrix layout of cm_off; one mbarrier per buffer counts the bytes.
+    auto issue_cb = [&](int c) {
+        uint64_t *cb = &sm.cbar[c & 1];
+        mbar_expect_tx(cb, 2u * kQ * kN * 2u);
+        const int g8 = (int)(((long long)b * L + (long long)c * kQ) / 8);
+        tma_load_4d(sm.C[c & 1], &tm_c, 0, 0, 0, g8, cb);
+        tma_load_4d(sm.B[c & 1], &tm_b, 0, 0, 0, g8, cb);
     };
     // x of chunk c: this thread's four 16-byte pieces, into registers
     constexpr int kXPieces = kQ * kP / 8 / kThreads;
@@ -402,13 +404,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
+        mbar_init(&sm.cbar[0], 1);
+        mbar_init(&sm.cbar[1], 1);
         fence_mbar_init();
     }
     uint4 xr[kXPieces];
     uint16_t dr[4] = {0, 0, 0, 0};
     float nd[4] = {0.f, 0.f, 0.f, 0.f}, nc[4] = {0.f, 0.f, 0.f, 0.f}, nw[4] = {0.f, 0.f, 0.f, 0.f};
+    // chunk c's C/B use buffer c & 1 for the (c / 2)-th time: its arrival is
+    // phase c / 2 of that buffer's barrier. Thread 0 tracks the last chunk whose
+    // loads it issued and the last it saw arrive.
+    int cb_issued = -1, cb_arrived = -1;
+    tc_fence_before();
+    __syncthreads();  // the barriers are initialised before the first TMA uses one
+    tc_fence_after();
     if (n_chunks > 0) {
-        for (int q = 0; q < 4; ++q) issue_cb(0, q);
+        if (tid == 0) {
+            issue_cb(0);
+            cb_issued = 0;
+        }
         load_x(0, xr);
         if (warp == 0) {
             load_dt(0, dr);
@@ -451,17 +465,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0) dt_put(nd, nc, nw);  // formed during the previous chunk
         // ---- the next chunk's operands start moving now
         const bool more = c + 1 < n_chunks;
+        bool cb_late = false;
+        if (tid == 0) {
+            if (more) {  // buffer (c + 1) & 1 was last read by chunk c - 1's products
+                issue_cb(c + 1);
+                cb_issued = c + 1;
+            }
+            // this chunk's C and B have landed
+            cb_late = !mbar_wait_bounded(&sm.cbar[c & 1], (c >> 1) & 1, p.wait_limit);
+            if (!cb_late) cb_arrived = c;
+        }
         if (more) {
-            issue_cb(c + 1, 0);
             load_x(c + 1, xr);
             if (warp == 0) load_dt(c + 1, dr);
-            cp_async_wait<1>();  // this chunk's C and B have landed
-        } else {
-            cp_async_wait<0>();
         }
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        if (__syncthreads_or(cb_late)) {
+            if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
+            timed_out = true;
+            break;
+        }
         tc_fence_after();
 
         // ---- G = C B^T into TMEM columns [0, 128)
@@ -472,7 +496,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_f16(tmem + kColG, dadv(dC, k * kKmStep), dadv(dB, k * kKmStep), kIdG, k > 0);
             mma_commit(&sm.bar);
         }
-        if (more) issue_cb(c + 1, 1);
         const float cum_last = sm.cum[kQ - 1];
         // ---- meanwhile: Xs (row s = r, this half's 4 pieces) and S scaled by
         // the chunk's decay in place (row r, this half's 32 columns)
@@ -556,7 +579,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (more) issue_cb(c + 1, 2);
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
@@ -581,7 +603,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // meanwhile: the next chunk's dt, running sum and block weights (its raw
         // dt was loaded at this chunk's start)
-        if (more) issue_cb(c + 1, 3);
         if (warp == 0 && more) dt_scan(dr, nd, nc, nw);
         if (__syncthreads_or(!mma_wait(&sm.bar, phase, p.wait_limit))) {
             if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
@@ -632,8 +653,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit();
         }
     }
-    if (tid == 0) bulk_wait_all();  // the y stores have completed
-    cp_async_wait<0>();  // nothing left in flight if a wait gave up
+    if (tid == 0) {
+        bulk_wait_all();  // the y stores have completed
+        // after a wait that gave up: C/B loads still in flight land before exit
+        for (int k = cb_arrived + 1; k <= cb_issued; ++k)
+            if (!mbar_wait_bounded(&sm.cbar[k & 1], (k >> 1) & 1, p.wait_limit)) break;
+    }
     // after a wait that gave up, give the committed products one more bounded
     // wait before their tensor memory is freed
     if (timed_out) mma_wait(&sm.bar, phase, p.wait_limit);
@@ -688,6 +713,24 @@ int ssd_tc_t(const ssh::SsdParams &p, cudaStream_t st) {
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return SS_ERR_UNSUPPORTED;
+    // C and B (batch, L, N) bf16 as 4D boxes (n mod 8, t mod 8, n / 8, t / 8):
+    // strides 2 B, 256 B, 16 B and 2048 B; a box of 8 x 8 x 16 x 16 is one
+    // 128 x 128 tile in core-matrix order
+    CUtensorMap tc_, tb_;
+    {
+        const cuuint64_t d4[4] = {8, 8, (cuuint64_t)kN / 8, (cuuint64_t)p.batch * p.seqlen / 8};
+        const cuuint64_t s4[3] = {(cuuint64_t)kN * 2, 16, (cuuint64_t)kN * 2 * 8};
+        const cuuint32_t b4[4] = {8, 8, (cuuint32_t)kN / 8, (cuuint32_t)kQ / 8};
+        const cuuint32_t e4[4] = {1, 1, 1, 1};
+        const void *bases[2] = {p.C, p.B};
+        CUtensorMap *maps[2] = {&tc_, &tb_};
+        for (int i = 0; i < 2; ++i)
+            if (fn(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(bases[i]), d4,
+                   s4, b4, e4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return SS_ERR_UNSUPPORTED;
+    }
     static bool done[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
@@ -697,18 +740,21 @@ int ssd_tc_t(const ssh::SsdParams &p, cudaStream_t st) {
             return SS_ERR_CUDA;
         done[dev] = true;
     }
-    kern<<<(unsigned)((long long)p.batch * p.heads), kThreads, smem, st>>>(tm, p);
+    kern<<<(unsigned)((long long)p.batch * p.heads), kThreads, smem, st>>>(tm, tc_, tb_, p);
     return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 }  // namespace
 
 bool ssh::ssd_tc_supported(const ssh::SsdParams &p) {
-    // y leaves by TMA: a 16-byte aligned base and (batch, step) rows indexable in 32 bits
+    // y, C and B move by TMA: 16-byte aligned bases and (batch, step) rows
+    // indexable in 32 bits
     return p.in_dtype == SS_BF16 && p.headdim == kP && p.dstate == kN && p.seqlen % kQ == 0 &&
            (long long)p.batch * p.heads < (1LL << 31) &&
            (long long)p.batch * p.seqlen < (1LL << 31) &&
-           (reinterpret_cast<uintptr_t>(p.y) & 15u) == 0 && encode_fn() != nullptr;
+           ((reinterpret_cast<uintptr_t>(p.y) | reinterpret_cast<uintptr_t>(p.B) |
+             reinterpret_cast<uintptr_t>(p.C)) & 15u) == 0 &&
+           encode_fn() != nullptr;
 }
 
 int ssh::launch_ssd_tc(const ssh::SsdParams &p, cudaStream_t st) {

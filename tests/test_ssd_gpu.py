@@ -77,19 +77,22 @@ def _oracle(c, batch, L, H, N, P=64, with_h0=True, softplus=True):
 @pytest.mark.parametrize("batch,L,H,N", [(2, 128, 3, 64), (1, 256, 2, 128), (2, 64, 1, 128),
                                          (1, 1024, 2, 128), (3, 384, 5, 128)])
 @pytest.mark.parametrize("with_h0", [True, False])
-@pytest.mark.parametrize("path", ["auto", "tcgen05"])
+@pytest.mark.parametrize("path", ["mma_sync", "tcgen05", "auto"])
 def test_ssd_matches_scan_oracle(batch, L, H, N, with_h0, path):
-    """Both kernels: the mma.sync one (the default) and the tensor-memory one
-    (dstate 128, seqlen % 128 == 0; other shapes are refused)."""
+    """Both kernels: the mma.sync one and the tensor-memory one (dstate 128,
+    seqlen % 128 == 0; other shapes are refused), and AUTO, which takes the
+    tensor-memory kernel where it applies and mma.sync elsewhere."""
     c = _case(200 + L + N + H, batch, L, H, N)
-    tc = path == "tcgen05"
-    ctx = _ctx(ss.SS_SSD_PATH_TCGEN05 if tc else ss.SS_SSD_PATH_AUTO)
-    if tc and not (N == 128 and L % 128 == 0):
+    tc_ok = N == 128 and L % 128 == 0
+    ctx = _ctx({"mma_sync": ss.SS_SSD_PATH_MMA_SYNC, "tcgen05": ss.SS_SSD_PATH_TCGEN05,
+                "auto": ss.SS_SSD_PATH_AUTO}[path])
+    if path == "tcgen05" and not tc_ok:
         with pytest.raises(ss.SSError) as ei:
             _run(c, ctx, with_h0)
         assert ei.value.status == ss.SS_ERR_UNSUPPORTED
         return
     y, hl = _run(c, ctx, with_h0)
+    tc = path == "tcgen05" or (path == "auto" and tc_ok)
     assert ctx.last_launch()[0] == (1 if tc else 0)
     y_ref, h_ref = _oracle(c, batch, L, H, N, with_h0=with_h0)
     check_close(y.cpu().numpy(), y_ref, True, "y")
@@ -122,7 +125,8 @@ def test_ssd_full_size_sampled_heads():
     batch, L, H, N = 8, 2048, 80, 128
     c = _case(217, batch, L, H, N)
     refs = {bh: _oracle(_sub(c, *bh), 1, L, 1, N) for bh in ((0, 0), (3, 41), (7, 79))}
-    for path, variant in ((ss.SS_SSD_PATH_AUTO, 0), (ss.SS_SSD_PATH_TCGEN05, 1)):
+    for path, variant in ((ss.SS_SSD_PATH_MMA_SYNC, 0), (ss.SS_SSD_PATH_TCGEN05, 1),
+                          (ss.SS_SSD_PATH_AUTO, 1)):
         ctx = _ctx(path)
         y, hl = _run(c, ctx)
         assert ctx.last_launch()[0] == variant
