@@ -19,10 +19,12 @@
 //
 // One CTA of 8 warps per (batch, head). Warp w reads TMEM lanes
 // [32 (w % 4), 32 (w % 4) + 32) (rows t of G, Y, Z; rows n of S) and takes half
-// w / 4 of each epilogue's columns. Thread 0 issues the MMAs and commits them
-// to one mbarrier; the other threads meanwhile build Xs and rescale S, and
-// warp 0 forms the next chunk's dt and its prefix sum while the Y, Z and S
-// products run. C and B are double-buffered and the next chunk's x and dt wait
+// w / 4 of each epilogue's columns. Thread 0 issues the MMAs: G, then at once
+// Z (it needs only C and the previous state), S as soon as Xs and the rescaled
+// state are in place, and Y after the mask; G and the chunk's last product
+// are committed to one mbarrier each, so Z and S run under the CUDA-core
+// phases (Xs, rescale, mask) and only Y is waited for at the end. Warp 0 forms
+// the next chunk's dt and its prefix sum while Y runs. C and B are double-buffered and the next chunk's x and dt wait
 // in registers, so a chunk's loads overlap the previous chunk's work. y leaves
 // through a 128-byte-swizzled shared tile (the masked tile's buffer, free once
 // Y is done) by TMA stores, whole rows at a time. The mask's exponentials
@@ -47,10 +49,11 @@ using namespace ssk;
 constexpr int kQ = 128;  // chunk length = MMA rows
 constexpr int kP = 64;   // head dimension
 constexpr int kN = 128;  // state size
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColG = 0;    // G (128 columns); then Z (C H_hi in 64, C H_lo in 64)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColG = 0;    // G (128 columns)
 constexpr uint32_t kColY = 128;  // Y (64)
 constexpr uint32_t kColS = 192;  // carried state S (64)
+constexpr uint32_t kColZ = 256;  // Z: C H_hi in 64, C H_lo in 64
 
 struct TcSmem {
     uint16_t C[2][kQ * kN];  // C of the chunk [t][n], K-major for G and Z (two buffers)
@@ -63,7 +66,9 @@ struct TcSmem {
     float dt[kQ];
     float cum[kQ];
     float W[kQ];  // exp2(cum_e - cum_s) dt_s, e the last step of s's 16-column block
-    uint64_t bar;
+    uint64_t bar;      // G of the chunk done
+    uint64_t bary;     // every product of the chunk done (committed after Y)
+    uint64_t bardrain; // after a wait that gave up: whatever was issued is done
     uint64_t cbar[2];  // TMA arrival of C and B into buffer 0 / 1
     uint32_t tmem;
 };
@@ -404,6 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
+        mbar_init(&sm.bary, 1);
+        mbar_init(&sm.bardrain, 1);
         mbar_init(&sm.cbar[0], 1);
         mbar_init(&sm.cbar[1], 1);
         fence_mbar_init();
@@ -495,6 +502,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < kN / 16; ++k)
                 mma_f16(tmem + kColG, dadv(dC, k * kKmStep), dadv(dB, k * kKmStep), kIdG, k > 0);
             mma_commit(&sm.bar);
+            // Z = C [H_hi | H_lo] (H written by the previous chunk, fenced at the chunk start)
+            const uint64_t dH = sdesc(sH, 0, kMn128Lbo, kMn128Sbo);
+#pragma unroll
+            for (int k = 0; k < kN / 16; ++k)
+                mma_f16(tmem + kColZ, dadv(dC, k * kKmStep), dadv(dH, k * kMn128Step), kIdZ, k > 0);
         }
         const float cum_last = sm.cum[kQ - 1];
         // ---- meanwhile: Xs (row s = r, this half's 4 pieces) and S scaled by
@@ -522,13 +534,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
         }
         if (tid == 0) bulk_wait_read();  // the previous chunk's y has left the M buffer
+        fence_proxy_async();  // Xs is visible to the tensor core
+        tc_fence_before();
         if (__syncthreads_or(!mma_wait(&sm.bar, phase, p.wait_limit))) {
             if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
             timed_out = true;
             break;
         }
-        phase ^= 1u;
         tc_fence_after();
+        // ---- S += B^T Xs (the rescaled state and Xs are in place)
+        if (tid == 0) {
+            const uint64_t dBt = sdesc(sB, 0, kMn128Lbo, kMn128Sbo);
+            const uint64_t dXs = sdesc(sXs, 0, kMn64Lbo, kMn64Sbo);
+#pragma unroll
+            for (int k = 0; k < kQ / 16; ++k)
+                mma_f16(tmem + kColS, dadv(dBt, k * kMn128Step), dadv(dXs, k * kMn64Step), kIdS, true);
+        }
 
         // ---- M = G o exp2(cum_t - cum_s) dt_s (s <= t), row t = r; the 16-column
         // pieces left of and on this quarter's band, alternately to the two halves
@@ -584,32 +605,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         tc_fence_after();
 
-        // ---- Y = M X, Z = C [H_hi | H_lo] (into G's columns), S += B^T Xs
+        // ---- Y = M X; the commit covers every product of the chunk
         if (tid == 0) {
             const uint64_t dM = sdesc(sM, 0, kKmLbo, kKmSbo), dX = sdesc(sX, 0, kMn64Lbo, kMn64Sbo);
-            const uint64_t dC = sdesc(sC, 0, kKmLbo, kKmSbo), dH = sdesc(sH, 0, kMn128Lbo, kMn128Sbo);
-            const uint64_t dBt = sdesc(sB, 0, kMn128Lbo, kMn128Sbo);
-            const uint64_t dXs = sdesc(sXs, 0, kMn64Lbo, kMn64Sbo);
 #pragma unroll
             for (int k = 0; k < kQ / 16; ++k)
                 mma_f16(tmem + kColY, dadv(dM, k * kKmStep), dadv(dX, k * kMn64Step), kIdY, k > 0);
-#pragma unroll
-            for (int k = 0; k < kN / 16; ++k)
-                mma_f16(tmem + kColG, dadv(dC, k * kKmStep), dadv(dH, k * kMn128Step), kIdZ, k > 0);
-#pragma unroll
-            for (int k = 0; k < kQ / 16; ++k)
-                mma_f16(tmem + kColS, dadv(dBt, k * kMn128Step), dadv(dXs, k * kMn64Step), kIdS, true);
-            mma_commit(&sm.bar);
+            mma_commit(&sm.bary);
         }
         // meanwhile: the next chunk's dt, running sum and block weights (its raw
         // dt was loaded at this chunk's start)
         if (warp == 0 && more) dt_scan(dr, nd, nc, nw);
-        if (__syncthreads_or(!mma_wait(&sm.bar, phase, p.wait_limit))) {
+        if (__syncthreads_or(!mma_wait(&sm.bary, phase, p.wait_limit))) {
             if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
             timed_out = true;
             break;
         }
-        phase ^= 1u;
+        phase ^= 1u;  // both barriers complete one phase per chunk
         tc_fence_after();
 
         // ---- y row t = r, this half's 32 channels, into the staging tile (the M
@@ -618,9 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = r;
             const float ft = ex2(sm.cum[t]);
             float y0[16], y1[16], zh0[16], zh1[16], zl0[16], zl1[16];
-            tmem_ld16x4(trow + kColY + c0, trow + kColY + c0 + 16, trow + kColG + c0,
-                        trow + kColG + c0 + 16, y0, y1, zh0, zh1);
-            tmem_ld16x2(trow + kColG + kP + c0, trow + kColG + kP + c0 + 16, zl0, zl1);
+            tmem_ld16x4(trow + kColY + c0, trow + kColY + c0 + 16, trow + kColZ + c0,
+                        trow + kColZ + c0 + 16, y0, y1, zh0, zh1);
+            tmem_ld16x2(trow + kColZ + kP + c0, trow + kColZ + kP + c0 + 16, zl0, zl1);
             auto finish = [&](int j, float (&yv)[16], const float (&zh)[16], const float (&zl)[16]) {
                 const uint4 x0 = *reinterpret_cast<const uint4 *>(sX + cm_off(t, c0 + 16 * j, kP));
                 const uint4 x1 = *reinterpret_cast<const uint4 *>(sX + cm_off(t, c0 + 16 * j + 8, kP));
@@ -659,9 +671,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = cb_arrived + 1; k <= cb_issued; ++k)
             if (!mbar_wait_bounded(&sm.cbar[k & 1], (k >> 1) & 1, p.wait_limit)) break;
     }
-    // after a wait that gave up, give the committed products one more bounded
-    // wait before their tensor memory is freed
-    if (timed_out) mma_wait(&sm.bar, phase, p.wait_limit);
+    // after a wait that gave up: one more commit tracks every product issued so
+    // far; give it a bounded wait before their tensor memory is freed
+    if (timed_out) {
+        if (tid == 0) mma_commit(&sm.bardrain);
+        mma_wait(&sm.bardrain, 0, p.wait_limit);
+    }
 
     if (p.h_last) {
         float v0[16], v1[16];
