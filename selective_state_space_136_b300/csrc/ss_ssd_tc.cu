@@ -17,21 +17,22 @@
 // where S[n][p] is the carried state, kept in fp32 in TMEM for the whole row
 // of chunks and copied to shared memory as bf16 hi + lo for the next Z.
 //
-// One CTA of 8 warps per (batch, head). Warp w reads TMEM lanes
-// [32 (w % 4), 32 (w % 4) + 32) (rows t of G, Y, Z; rows n of S) and takes half
-// w / 4 of each epilogue's columns. Thread 0 issues the MMAs: G, then at once
-// Z (it needs only C and the previous state), S as soon as Xs and the rescaled
-// state are in place, and Y after the mask; G and the chunk's last product
-// are committed to one mbarrier each, so Z and S run under the CUDA-core
-// phases (Xs, rescale, mask) and only Y is waited for at the end. Warp 0 forms
-// the next chunk's dt and its prefix sum while Y runs. C and B are double-buffered and the next chunk's x and dt wait
-// in registers, so a chunk's loads overlap the previous chunk's work. y leaves
-// through a 128-byte-swizzled shared tile (the masked tile's buffer, free once
-// Y is done) by TMA stores, whole rows at a time. The mask's exponentials
-// below the diagonal 32 x 32 band are factored per 16-column block with end e:
-// exp2(cum_t - cum_s) = exp2(cum_t - cum_e) exp2(cum_e - cum_s), both factors
-// at most 1 (cum falls along the chunk), one exponential per row and block
-// plus one per column, instead of one per element. Shared
+// One CTA of 16 warps per (batch, head). Warp w reads TMEM lanes
+// [32 (w % 4), 32 (w % 4) + 32) (rows t of G, Y, Z; rows n of S) and takes
+// part w / 4 of four of each epilogue's columns. Thread 0 issues the MMAs: G,
+// then at once Z (it needs only C and the previous state), S as soon as Xs and
+// the rescaled state are in place, and Y after the mask; G and the chunk's
+// last product are committed to one mbarrier each, so Z and S run under the
+// CUDA-core phases (Xs, rescale, mask) and only Y is waited for at the end.
+// Warp 0 forms the next chunk's dt and its prefix sum while Y runs. C and B
+// arrive by TMA into two buffers, the next chunk's issued at this one's start;
+// the next chunk's x waits in registers.
+// y leaves through a 128-byte-swizzled shared tile (the masked tile's buffer,
+// free once Y is done) by TMA stores, whole rows at a time. The mask's
+// exponentials below the diagonal 32 x 32 band are factored per 16-column
+// block with end e: exp2(cum_t - cum_s) = exp2(cum_t - cum_e) exp2(cum_e -
+// cum_s), both factors at most 1 (cum falls along the chunk), one exponential
+// per row and block plus one per column, instead of one per element. Shared
 // operand tiles are stored as 8-row x 16-byte core matrices, column blocks
 // fastest, and described to the tensor core without swizzling: K-major tiles
 // (C, B, M) with the leading offset between K-adjacent core matrices and the
@@ -160,17 +161,17 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t a0, uint32_t a1, float (&v0
 #pragma unroll
     for (int i = 0; i < 16; ++i) v1[i] = __uint_as_float(r[16 + i]);
 }
-// 4 x 16 fp32 columns of this thread's TMEM lane with one wait for all.
-__device__ __forceinline__ void tmem_ld16x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, float (&v0)[16], float (&v1)[16], float (&v2)[16], float (&v3)[16]) {
-    uint32_t r[64];
+// 3 x 16 fp32 columns of this thread's TMEM lane with one wait for all.
+__device__ __forceinline__ void tmem_ld16x3(uint32_t a0, uint32_t a1, uint32_t a2, float (&v0)[16],
+                                            float (&v1)[16], float (&v2)[16]) {
+    uint32_t r[48];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%64];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%65];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%66];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%67];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%48];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%49];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%50];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47])
+        : "r"(a0), "r"(a1), "r"(a2)
         : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v0[i] = __uint_as_float(r[0 + i]);
@@ -178,8 +179,6 @@ __device__ __forceinline__ void tmem_ld16x4(uint32_t a0, uint32_t a1, uint32_t a
     for (int i = 0; i < 16; ++i) v1[i] = __uint_as_float(r[16 + i]);
 #pragma unroll
     for (int i = 0; i < 16; ++i) v2[i] = __uint_as_float(r[32 + i]);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v3[i] = __uint_as_float(r[48 + i]);
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
     asm volatile(
@@ -300,8 +299,10 @@ __device__ __forceinline__ void stage16(uint8_t *st, int t, int c, const float (
     *reinterpret_cast<uint4 *>(st + sw128(t, j0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-constexpr int kThreads = 256;  // 8 warps: warp w serves TMEM lanes 32 (w % 4) .. +32 and
-                               // column half w / 4 of each epilogue
+constexpr int kThreads = 512;  // 16 warps: warp w serves TMEM lanes 32 (w % 4) .. +32 and
+                               // column part w / 4 of each epilogue
+constexpr int kParts = kThreads / 128;  // warps per TMEM lane quarter
+constexpr int kCols = kP / kParts;      // this thread's columns of Y, Z and S
 
 template <typename Tout>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sH = reinterpret_cast<uint8_t *>(sm.H);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, part = warp >> 2;
     const int r = 32 * quarter + lane;  // this thread's TMEM lane: row t of G, Y, Z; row n of S
     const int b = blockIdx.x / p.heads, h = blockIdx.x % p.heads;
     const long long L = p.seqlen;
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows of one core matrix (distinct banks). Block k of warp w is block
     // w + 8 k of the tile's (rows / 8) x (pieces / 4) blocks, pieces fastest.
     auto piece = [&](int k, int blocks_per_row_group, int &row, int &pc) {
-        const int blk = warp + 8 * k;
+        const int blk = warp + (kThreads / 32) * k;
         row = 8 * (blk / blocks_per_row_group) + (lane & 7);
         pc = 4 * (blk % blocks_per_row_group) + (lane >> 3);
     };
@@ -441,11 +442,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
     const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);  // this warp's lanes
-    const int c0 = 32 * half;  // this thread's columns of Y, Z and S
+    const int c0 = kCols * part;  // this thread's columns of Y, Z and S
 
-    // initial state: row n = r, columns [c0, c0 + 32) of S (tensor memory) and of H
+    // initial state: row n = r, columns [c0, c0 + kCols) of S (tensor memory) and of H
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < kCols / 16; ++j) {
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -470,9 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4 *>(sX + cm_off(s, 8 * p8, kP)) = xr[k];
         }
         if (warp == 0) dt_put(nd, nc, nw);  // formed during the previous chunk
-        // ---- the next chunk's operands start moving now
         const bool more = c + 1 < n_chunks;
         bool cb_late = false;
+        // ---- the next chunk's operands start moving now
         if (tid == 0) {
             if (more) {  // buffer (c + 1) & 1 was last read by chunk c - 1's products
                 issue_cb(c + 1);
@@ -509,14 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_f16(tmem + kColZ, dadv(dC, k * kKmStep), dadv(dH, k * kMn128Step), kIdZ, k > 0);
         }
         const float cum_last = sm.cum[kQ - 1];
-        // ---- meanwhile: Xs (row s = r, this half's 4 pieces) and S scaled by
-        // the chunk's decay in place (row r, this half's 32 columns)
+        // ---- meanwhile: Xs (row s = r, this part's pieces) and S scaled by
+        // the chunk's decay in place (row r, this part's columns)
         {
             const int s = r;
             const float w = ex2(cum_last - sm.cum[s]) * sm.dt[s];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int p8 = 4 * half + k;
+            for (int k = 0; k < kP / 8 / kParts; ++k) {
+                const int p8 = (kP / 8 / kParts) * part + k;
                 const uint4 v = *reinterpret_cast<const uint4 *>(sX + cm_off(s, 8 * p8, kP));
                 const uint4 o = make_uint4(pack2(bf16lo(v.x) * w, bf16hi(v.x) * w),
                                            pack2(bf16lo(v.y) * w, bf16hi(v.y) * w),
@@ -525,12 +526,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(sXs + cm_off(s, 8 * p8, kP)) = o;
             }
             const float dec = ex2(cum_last);
-            float v0[16], v1[16];
-            tmem_ld16x2(trow + kColS + c0, trow + kColS + c0 + 16, v0, v1);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v0[i] *= dec, v1[i] *= dec;
-            tmem_st16(trow + kColS + c0, v0);
-            tmem_st16(trow + kColS + c0 + 16, v1);
+            for (int j = 0; j < kCols / 16; ++j) {
+                float v0[16];
+                tmem_ld16(trow + kColS + c0 + 16 * j, v0);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v0[i] *= dec;
+                tmem_st16(trow + kColS + c0 + 16 * j, v0);
+            }
             tmem_wait_st();
         }
         if (tid == 0) bulk_wait_read();  // the previous chunk's y has left the M buffer
@@ -552,11 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---- M = G o exp2(cum_t - cum_s) dt_s (s <= t), row t = r; the 16-column
-        // pieces left of and on this quarter's band, alternately to the two halves
+        // pieces left of and on this quarter's band, dealt round the parts
         {
             const int t = r;
             const float ct = sm.cum[t];
-            // this warp's pieces j = half, half + 2, ... (quarter + 1 of them), two per load
+            // this warp's pieces j = part, part + kParts, ... below 2 (quarter + 1), two per load
             // pieces left of the band (s0 + 16 <= 32 quarter <= t for every lane of
             // the warp) take the factored form; the band's two pieces the direct one
             auto mask_piece = [&](int s0, const float (&g)[16]) {
@@ -584,15 +587,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_uint4(w[4], w[5], w[6], w[7]);
             };
             // right of the band s > t: zeros (the buffer held the last chunk's y)
-            for (int s8 = 4 * (quarter + 1) + half; s8 < kQ / 8; s8 += 2)
+            for (int s8 = 4 * (quarter + 1) + part; s8 < kQ / 8; s8 += kParts)
                 *reinterpret_cast<uint4 *>(sM + cm_off(t, 8 * s8, kQ)) = make_uint4(0u, 0u, 0u, 0u);
-            for (int k = 0; k <= quarter; k += 2) {
-                const int s0 = 16 * (half + 2 * k);
-                if (k + 1 <= quarter) {
+            const int np = 2 * (quarter + 1);
+            for (int j = part; j < np; j += 2 * kParts) {
+                const int s0 = 16 * j;
+                if (j + kParts < np) {
                     float g0[16], g1[16];
-                    tmem_ld16x2(trow + kColG + s0, trow + kColG + s0 + 32, g0, g1);
+                    tmem_ld16x2(trow + kColG + s0, trow + kColG + s0 + 16 * kParts, g0, g1);
                     mask_piece(s0, g0);
-                    mask_piece(s0 + 32, g1);
+                    mask_piece(s0 + 16 * kParts, g1);
                 } else {
                     float g0[16];
                     tmem_ld16(trow + kColG + s0, g0);
@@ -624,15 +628,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         phase ^= 1u;  // both barriers complete one phase per chunk
         tc_fence_after();
 
-        // ---- y row t = r, this half's 32 channels, into the staging tile (the M
+        // ---- y row t = r, this part's channels, into the staging tile (the M
         // buffer) and out by TMA; the new state's row n = r (same columns) into H
         {
             const int t = r;
             const float ft = ex2(sm.cum[t]);
-            float y0[16], y1[16], zh0[16], zh1[16], zl0[16], zl1[16];
-            tmem_ld16x4(trow + kColY + c0, trow + kColY + c0 + 16, trow + kColZ + c0,
-                        trow + kColZ + c0 + 16, y0, y1, zh0, zh1);
-            tmem_ld16x2(trow + kColZ + kP + c0, trow + kColZ + kP + c0 + 16, zl0, zl1);
             auto finish = [&](int j, float (&yv)[16], const float (&zh)[16], const float (&zl)[16]) {
                 const uint4 x0 = *reinterpret_cast<const uint4 *>(sX + cm_off(t, c0 + 16 * j, kP));
                 const uint4 x1 = *reinterpret_cast<const uint4 *>(sX + cm_off(t, c0 + 16 * j + 8, kP));
@@ -645,12 +645,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 stage16(sM, t, c0 + 16 * j, yv, Tout());
             };
-            finish(0, y0, zh0, zl0);
-            finish(1, y1, zh1, zl1);
-            float v0[16], v1[16];
-            tmem_ld16x2(trow + kColS + c0, trow + kColS + c0 + 16, v0, v1);
-            put_state16(sH, t, c0, v0);
-            put_state16(sH, t, c0 + 16, v1);
+#pragma unroll
+            for (int j = 0; j < kCols / 16; ++j) {
+                float y0[16], zh0[16], zl0[16];
+                tmem_ld16x3(trow + kColY + c0 + 16 * j, trow + kColZ + c0 + 16 * j,
+                            trow + kColZ + kP + c0 + 16 * j, y0, zh0, zl0);
+                finish(j, y0, zh0, zl0);
+                float v0[16];
+                tmem_ld16(trow + kColS + c0 + 16 * j, v0);
+                put_state16(sH, t, c0 + 16 * j, v0);
+            }
         }
         fence_proxy_async();  // the staged y is visible to the TMA unit
         __syncthreads();
@@ -679,12 +683,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (p.h_last) {
-        float v0[16], v1[16];
-        tmem_ld16x2(trow + kColS + c0, trow + kColS + c0 + 16, v0, v1);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            p.h_last[st_base + (long long)(c0 + i) * kN + r] = v0[i];
-            p.h_last[st_base + (long long)(c0 + 16 + i) * kN + r] = v1[i];
+        for (int j = 0; j < kCols / 16; ++j) {
+            float v0[16];
+            tmem_ld16(trow + kColS + c0 + 16 * j, v0);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) p.h_last[st_base + (long long)(c0 + 16 * j + i) * kN + r] = v0[i];
         }
     }
     tc_fence_before();
