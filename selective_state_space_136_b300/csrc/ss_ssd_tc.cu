@@ -496,18 +496,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 
-        // ---- G = C B^T into TMEM columns [0, 128)
-        if (tid == 0) {
+        // ---- G = C B^T into TMEM columns [0, 128). The descriptors are formed by
+        // the whole of warp 0 (warp-uniform values) and lane 0 issues.
+        if (warp == 0) {
             const uint64_t dC = sdesc(sC, 0, kKmLbo, kKmSbo), dB = sdesc(sB, 0, kKmLbo, kKmSbo);
-#pragma unroll
-            for (int k = 0; k < kN / 16; ++k)
-                mma_f16(tmem + kColG, dadv(dC, k * kKmStep), dadv(dB, k * kKmStep), kIdG, k > 0);
-            mma_commit(&sm.bar);
-            // Z = C [H_hi | H_lo] (H written by the previous chunk, fenced at the chunk start)
             const uint64_t dH = sdesc(sH, 0, kMn128Lbo, kMn128Sbo);
+            if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < kN / 16; ++k)
-                mma_f16(tmem + kColZ, dadv(dC, k * kKmStep), dadv(dH, k * kMn128Step), kIdZ, k > 0);
+                for (int k = 0; k < kN / 16; ++k)
+                    mma_f16(tmem + kColG, dadv(dC, k * kKmStep), dadv(dB, k * kKmStep), kIdG, k > 0);
+                mma_commit(&sm.bar);
+                // Z = C [H_hi | H_lo] (H written by the previous chunk, fenced at the chunk start)
+#pragma unroll
+                for (int k = 0; k < kN / 16; ++k)
+                    mma_f16(tmem + kColZ, dadv(dC, k * kKmStep), dadv(dH, k * kMn128Step), kIdZ, k > 0);
+            }
+            __syncwarp();
         }
         const float cum_last = sm.cum[kQ - 1];
         // ---- meanwhile: Xs (row s = r, this part's pieces) and S scaled by
@@ -546,12 +550,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         // ---- S += B^T Xs (the rescaled state and Xs are in place)
-        if (tid == 0) {
+        if (warp == 0) {
             const uint64_t dBt = sdesc(sB, 0, kMn128Lbo, kMn128Sbo);
             const uint64_t dXs = sdesc(sXs, 0, kMn64Lbo, kMn64Sbo);
+            if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < kQ / 16; ++k)
-                mma_f16(tmem + kColS, dadv(dBt, k * kMn128Step), dadv(dXs, k * kMn64Step), kIdS, true);
+                for (int k = 0; k < kQ / 16; ++k)
+                    mma_f16(tmem + kColS, dadv(dBt, k * kMn128Step), dadv(dXs, k * kMn64Step), kIdS, true);
+            }
+            __syncwarp();
         }
 
         // ---- M = G o exp2(cum_t - cum_s) dt_s (s <= t), row t = r; the 16-column
@@ -610,12 +617,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 
         // ---- Y = M X; the commit covers every product of the chunk
-        if (tid == 0) {
+        if (warp == 0) {
             const uint64_t dM = sdesc(sM, 0, kKmLbo, kKmSbo), dX = sdesc(sX, 0, kMn64Lbo, kMn64Sbo);
+            if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < kQ / 16; ++k)
-                mma_f16(tmem + kColY, dadv(dM, k * kKmStep), dadv(dX, k * kMn64Step), kIdY, k > 0);
-            mma_commit(&sm.bary);
+                for (int k = 0; k < kQ / 16; ++k)
+                    mma_f16(tmem + kColY, dadv(dM, k * kKmStep), dadv(dX, k * kMn64Step), kIdY, k > 0);
+                mma_commit(&sm.bary);
+            }
+            __syncwarp();
         }
         // meanwhile: the next chunk's dt, running sum and block weights (its raw
         // dt was loaded at this chunk's start)
