@@ -672,6 +672,343 @@ __global__ void __launch_bounds__(32, ZH ? 8 : 9) scan_bwd2_kernel(const ssh::Bw
     }
 }
 
+// dstate 16 with a row's states over two lanes: lane 2 i + q of a warp serves
+// row i of its 16 and states [8 q, 8 q + 8) as four pairs, so a 32-channel row
+// block is a CTA of two warps (twice the warps of the one-lane-per-row kernels
+// for the same rows: the walk's per-step chains are the limit there, and more
+// warps hide more of them). Both lanes of a row compute the row's scalars (dt,
+// the gate, the sums over states after one xor-shuffle); dB and dC are summed
+// over the warp's 16 rows by a four-level reduce-scatter, after which lane
+// 2 i + q holds value i of its half (dB for i < 8, dC otherwise) and adds it
+// with one atomic. The CTA's two warps share one B/C tile. At 18 warps per SM
+// the kernel has 96 registers a thread (some spill); it is taken where the
+// extra work per state makes the one-lane-per-row kernel slower (the exact
+// zero-order hold).
+struct BwdSmemSplit {
+    float bc[kTL][32];  // B (n < 16), C (n >= 16) of the tile, fp32
+    struct PerWarp {
+        float2 S[kHalf - 1][4][32];  // recomputed states but the last, pairs per lane
+        // per row: dt, u, z, dy of each step; once step t has been walked back
+        // its slots take ddelta, du and dz
+        float io[4][kTL][16];
+    } w[2];
+};
+
+template <typename Tin, bool ZH>
+__global__ void __launch_bounds__(64, 9) scan_bwd_split_kernel(const ssh::BwdParams p) {
+    constexpr int N = 16, NP = 4;
+    constexpr unsigned FULL = 0xffffffffu;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    BwdSmemSplit &sm = *reinterpret_cast<BwdSmemSplit *>(smem_raw);
+    const int tid = threadIdx.x, wi = tid >> 5, lane = tid & 31;
+    const int rr = lane >> 1, q = lane & 1, n0 = 8 * q;
+    BwdSmemSplit::PerWarp &wm = sm.w[wi];
+    const int rb_per_batch = (p.dim + 31) / 32;
+    const int b = blockIdx.x / rb_per_batch, blk = blockIdx.x % rb_per_batch;
+    const int d = blk * 32 + wi * 16 + rr;
+    const bool row_ok = d < p.dim;
+    const int dc = row_ok ? d : p.dim - 1;
+    const long long row = (long long)b * p.dim + dc;
+    const long long L = p.seqlen;
+    const int K = (int)(L / kTL);
+
+    f2 Ar[NP];  // A of this lane's states, pairs; exp(dt a) is taken as ex2((dt log2 e) a)
+#pragma unroll
+    for (int j = 0; j < NP; ++j)
+        Ar[j] = mk2(p.A[(long long)dc * N + n0 + 2 * j], p.A[(long long)dc * N + n0 + 2 * j + 1]);
+    f2 iA[ZH ? NP : 1];  // 1 / A (0 where A = 0)
+#pragma unroll
+    for (int j = 0; j < (ZH ? NP : 1); ++j)
+        iA[j] = mk2(Ar[j].x != 0.f ? 1.f / Ar[j].x : 0.f, Ar[j].y != 0.f ? 1.f / Ar[j].y : 0.f);
+    const float bias = p.bias ? p.bias[dc] : 0.f;
+    const float Dd = p.D ? p.D[dc] : 0.f;
+    const Tin *gu = static_cast<const Tin *>(p.u) + row * L;
+    const Tin *gd = static_cast<const Tin *>(p.delta) + row * L;
+    const Tin *gz = p.z ? static_cast<const Tin *>(p.z) + row * L : nullptr;
+    // checkpoints: per row slot (32 per CTA) K tiles of N floats; this lane's 8
+    float *ck = p.ckpt + ((long long)blockIdx.x * 32 + wi * 16 + rr) * (long long)K * N + n0;
+
+    // the CTA's B/C tile: warp 0's lane i reads row i % 16 of B (i < 16) or C
+    auto bc_load = [&](long long l0) {
+        __syncthreads();
+        if (wi == 0) {
+            const Tin *src = static_cast<const Tin *>(lane < N ? p.B : p.C) +
+                             ((long long)b * N + (lane % N)) * L + l0;
+            float v[kTL];
+            load_tile(src, v);
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) sm.bc[t][lane] = v[t];
+        }
+        __syncthreads();
+    };
+    auto Bpair = [&](int t, int j) {
+        const float2 v = *reinterpret_cast<const float2 *>(&sm.bc[t][n0 + 2 * j]);
+        return mk2(v.x, v.y);
+    };
+    auto Cpair = [&](int t, int j) {
+        const float2 v = *reinterpret_cast<const float2 *>(&sm.bc[t][N + n0 + 2 * j]);
+        return mk2(v.x, v.y);
+    };
+    // one forward step of this lane's states; du is dt * u (simplified) or u (zero-order hold)
+    auto fwd_step = [&](f2 *h, float dt, float du, int t) {
+        const float dl = dt * kLog2e;
+        const f2 dd = mk2(dl, dl), uu = mk2(du, du);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const f2 tt = fmul2(dd, Ar[j]);
+            const f2 e = mk2(ex2(tt.x), ex2(tt.y));
+            if constexpr (ZH) {
+                const f2 dn = mk2(dt, dt);
+                const f2 f = zoh_f2(dn, fmul2(dn, Ar[j]), e, iA[j]);
+                h[j] = ffma2(e, h[j], fmul2(fmul2(f, uu), Bpair(t, j)));
+            } else {
+                h[j] = ffma2(e, h[j], fmul2(uu, Bpair(t, j)));
+            }
+        }
+    };
+    auto step_in = [&](float dt, float u) { return ZH ? u : dt * u; };
+
+    // ---- forward sweep: the state entering every tile
+    {
+        f2 h[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j)
+            h[j] = p.h0 ? mk2(p.h0[row * N + n0 + 2 * j], p.h0[row * N + n0 + 2 * j + 1]) : mk2(0.f, 0.f);
+        for (int k = 0; k < K; ++k) {
+            const long long l0 = (long long)k * kTL;
+#pragma unroll
+            for (int j = 0; j < NP; ++j)
+                *reinterpret_cast<float2 *>(ck + (long long)k * N + 2 * j) = make_float2(h[j].x, h[j].y);
+            bc_load(l0);
+            float uv[kTL], dl[kTL];
+            load_tile(gu + l0, uv);
+            load_tile(gd + l0, dl);
+#pragma unroll
+            for (int t = 0; t < kTL; ++t) {
+                const float x = dl[t] + bias;
+                const float dt = p.softplus ? softplus1(x) : x;
+                fwd_step(h, dt, step_in(dt, uv[t]), t);
+            }
+        }
+    }
+
+    // ---- reverse sweep
+    f2 g[NP], gA[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        g[j] = (row_ok && p.dh_last)
+                   ? mk2(p.dh_last[row * N + n0 + 2 * j], p.dh_last[row * N + n0 + 2 * j + 1])
+                   : mk2(0.f, 0.f);
+        gA[j] = mk2(0.f, 0.f);
+    }
+    float gD = 0.f, gbias = 0.f;
+    for (int k = K - 1; k >= 0; --k) {
+        const long long l0 = (long long)k * kTL;
+        bc_load(l0);
+        {
+            // lane q = 0 stages the row's dt and u, lane q = 1 its z and dy
+            float v0[kTL], v1[kTL];
+            if (q == 0) {
+                load_tile(gu + l0, v0);
+                load_tile(gd + l0, v1);
+#pragma unroll
+                for (int t = 0; t < kTL; ++t) {
+                    const float x = v1[t] + bias;
+                    wm.io[0][t][rr] = p.softplus ? softplus1(x) : x;
+                    wm.io[1][t][rr] = v0[t];
+                }
+            } else {
+                if (gz) {
+                    load_tile(gz + l0, v0);
+#pragma unroll
+                    for (int t = 0; t < kTL; ++t) wm.io[2][t][rr] = v0[t];
+                }
+                load_tile(p.dy + row * L + l0, v1);
+#pragma unroll
+                for (int t = 0; t < kTL; ++t) wm.io[3][t][rr] = row_ok ? v1[t] : 0.f;
+            }
+        }
+        __syncwarp();
+
+#pragma unroll 1
+        for (int half = 1; half >= 0; --half) {
+            const int t0 = half * kHalf;
+            f2 hp[NP];  // the tile's checkpoint, read again for each half (fewer live registers)
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const float2 v = *reinterpret_cast<const float2 *>(ck + (long long)k * N + 2 * j);
+                hp[j] = mk2(v.x, v.y);
+            }
+            if (half == 1) {
+#pragma unroll 1
+                for (int t = 0; t < kHalf; ++t) {
+                    const float dtt = wm.io[0][t][rr];
+                    fwd_step(hp, dtt, step_in(dtt, wm.io[1][t][rr]), t);
+                }
+            }
+            f2 hcur[NP];  // after the loop: the state after the half's last step
+#pragma unroll
+            for (int j = 0; j < NP; ++j) hcur[j] = hp[j];
+#pragma unroll 1
+            for (int t = 0; t < kHalf; ++t) {
+                const float dtt = wm.io[0][t0 + t][rr];
+                fwd_step(hcur, dtt, step_in(dtt, wm.io[1][t0 + t][rr]), t0 + t);
+                if (t < kHalf - 1) {
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) wm.S[t][j][lane] = make_float2(hcur[j].x, hcur[j].y);
+                }
+            }
+            __syncwarp();
+#pragma unroll 1
+            for (int t = kHalf - 1; t >= 0; --t) {
+                const int tt = t0 + t;
+                const float dtt = wm.io[0][tt][rr], u = wm.io[1][tt][rr];
+                const float dyt = wm.io[3][tt][rr];
+                f2 hprev[NP];
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const float2 v = t > 0 ? wm.S[t - 1][j][lane] : make_float2(hp[j].x, hp[j].y);
+                    hprev[j] = mk2(v.x, v.y);
+                }
+                f2 s2 = mk2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) s2 = ffma2(Cpair(tt, j), hcur[j], s2);
+                float s = s2.x + s2.y;
+                s += __shfl_xor_sync(FULL, s, 1);
+                s = fmaf(Dd, u, s);
+                float gs = dyt;
+                if (gz) {
+                    const float zz = wm.io[2][tt][rr];
+                    const float sg = __fdividef(1.f, 1.f + ex2(-zz * kLog2e));
+                    const float dzv = dyt * s * sg * fmaf(zz, 1.f - sg, 1.f);
+                    __syncwarp();
+                    if (q == 0) wm.io[2][tt][rr] = dzv;
+                    gs = dyt * zz * sg;
+                }
+                gD = fmaf(gs, u, gD);
+                const float dl = dtt * kLog2e;
+                const f2 gs2 = mk2(gs, gs), dd = mk2(dtt, dtt), dd2 = mk2(dl, dl), uu = mk2(u, u);
+                f2 gu2 = mk2(0.f, 0.f), gdt2 = mk2(0.f, 0.f);
+                float v[16];  // this lane's dB (i < 8) and dC (i >= 8) terms of the step
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const f2 Bp = Bpair(tt, j), Cp = Cpair(tt, j);
+                    const f2 tq = fmul2(dd2, Ar[j]);
+                    const f2 e = mk2(ex2(tq.x), ex2(tq.y));
+                    g[j] = ffma2(gs2, Cp, g[j]);
+                    const f2 vc = fmul2(gs2, hcur[j]);
+                    v[8 + 2 * j] = vc.x, v[8 + 2 * j + 1] = vc.y;
+                    const f2 ehp = fmul2(e, hprev[j]);
+                    if constexpr (ZH) {
+                        f2 fa;
+                        const f2 f = zoh_factor2(dd, fmul2(dd, dd), fmul2(dd, Ar[j]), e, iA[j], &fa);
+                        const f2 gf = fmul2(g[j], f);
+                        const f2 vb = fmul2(gf, uu);
+                        v[2 * j] = vb.x, v[2 * j + 1] = vb.y;
+                        gu2 = ffma2(gf, Bp, gu2);
+                        const f2 bu = fmul2(Bp, uu);
+                        gdt2 = ffma2(g[j], ffma2(Ar[j], ehp, fmul2(e, bu)), gdt2);
+                        gA[j] = ffma2(g[j], ffma2(dd, ehp, fmul2(fa, bu)), gA[j]);
+                    } else {
+                        const f2 gdu = fmul2(g[j], dd);
+                        const f2 vb = fmul2(gdu, uu);
+                        v[2 * j] = vb.x, v[2 * j + 1] = vb.y;
+                        gu2 = ffma2(gdu, Bp, gu2);
+                        gdt2 = ffma2(g[j], ffma2(Ar[j], ehp, fmul2(Bp, uu)), gdt2);
+                        gA[j] = ffma2(gdu, ehp, gA[j]);
+                    }
+                    g[j] = fmul2(g[j], e);
+                    hcur[j] = hprev[j];
+                }
+                float gdt = gdt2.x + gdt2.y;
+                gdt += __shfl_xor_sync(FULL, gdt, 1);
+                float gu_ = gu2.x + gu2.y;
+                gu_ += __shfl_xor_sync(FULL, gu_, 1);
+                gu_ = fmaf(gs, Dd, gu_);
+                // softplus'(x) = sigmoid(x) = 1 - exp(-softplus(x))
+                const float gx = p.softplus ? gdt * -expm1f(-dtt) : gdt;
+                gbias += gx;
+                __syncwarp();
+                if (q == 0) {
+                    wm.io[1][tt][rr] = gu_;
+                    wm.io[0][tt][rr] = gx;
+                }
+                // dB and dC of the step summed over the warp's 16 rows (lanes of
+                // one q): halving exchanges over lane bits 4..1; lane 2 i + q
+                // ends with value i of its half
+#pragma unroll
+                for (int m = 16, c = 16; m >= 2; m >>= 1, c >>= 1) {
+                    const bool upper = (lane & m) != 0;
+#pragma unroll
+                    for (int i = 0; i < c / 2; ++i) {
+                        const float send = upper ? v[i] : v[i + c / 2];
+                        const float keep = upper ? v[i + c / 2] : v[i];
+                        v[i] = keep + __shfl_xor_sync(FULL, send, m);
+                    }
+                }
+                {
+                    const int i = rr;  // value index held by this lane
+                    float *dst = (i < 8 ? p.dB : p.dC) + ((long long)b * N + n0 + (i & 7)) * L + l0 + tt;
+                    atomicAdd(dst, v[0]);
+                }
+            }
+            __syncwarp();
+        }
+        __syncwarp();
+        if (row_ok) {
+            float o[kTL];
+            if (q == 0) {
+#pragma unroll
+                for (int t = 0; t < kTL; ++t) o[t] = wm.io[1][t][rr];
+                store_tile16(p.du + row * L + l0, o);
+#pragma unroll
+                for (int t = 0; t < kTL; ++t) o[t] = wm.io[0][t][rr];
+                store_tile16(p.ddelta + row * L + l0, o);
+            } else if (p.dz) {
+#pragma unroll
+                for (int t = 0; t < kTL; ++t) o[t] = wm.io[2][t][rr];
+                store_tile16(p.dz + row * L + l0, o);
+            }
+        }
+    }
+    if (row_ok) {
+        if (p.dh0) {
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                p.dh0[row * N + n0 + 2 * j] = g[j].x;
+                p.dh0[row * N + n0 + 2 * j + 1] = g[j].y;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            atomicAdd(p.dA + (long long)dc * N + n0 + 2 * j, gA[j].x);
+            atomicAdd(p.dA + (long long)dc * N + n0 + 2 * j + 1, gA[j].y);
+        }
+        if (q == 0) {
+            if (p.dD) atomicAdd(p.dD + dc, gD);
+            if (p.dbias) atomicAdd(p.dbias + dc, gbias);
+        }
+    }
+}
+
+template <typename Tin, bool ZH>
+int bwd_launch_split(const ssh::BwdParams &p, cudaStream_t st) {
+    auto kern = scan_bwd_split_kernel<Tin, ZH>;
+    const int smem = (int)sizeof(BwdSmemSplit);
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return SS_ERR_CUDA;
+        attr_done[dev] = true;
+    }
+    const long long blocks = (long long)p.batch * ((p.dim + 31) / 32);
+    kern<<<(unsigned)blocks, 64, smem, st>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
 // One instantiation (and so one attribute cache) per kernel: ZH is part of the key.
 template <typename Tin, int N, typename Smem, bool ZH, typename Kern>
 int bwd_launch(Kern kern, const ssh::BwdParams &p, cudaStream_t st) {
@@ -693,6 +1030,11 @@ int bwd_launch(Kern kern, const ssh::BwdParams &p, cudaStream_t st) {
 template <typename Tin, int N>
 int bwd_n(const ssh::BwdParams &p, cudaStream_t st) {
     if constexpr (SS_BWD_PACKED && N % 2 == 0) {
+        // dstate 16 with the zero-order hold: the state-split kernel (5.26 ms
+        // against 6.18 at (8, 5120, 16, 2048); for the simplified form it
+        // measured 3.39 ms against the packed kernel's 3.32)
+        if constexpr (N == 16)
+            if (p.zoh) return bwd_launch_split<Tin, true>(p, st);
         if (p.zoh)
             return bwd_launch<Tin, N, BwdSmem2<N>, true>(scan_bwd2_kernel<Tin, N, true>, p, st);
         return bwd_launch<Tin, N, BwdSmem2<N>, false>(scan_bwd2_kernel<Tin, N, false>, p, st);
