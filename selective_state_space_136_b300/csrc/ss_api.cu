@@ -260,10 +260,13 @@ int run_pair(ss_ctx *ctx, const ssh::ScanParams &p, bool chunked, cudaStream_t s
                                    ctx->sm_count;
         int req = ctx->segments;
         if (req <= 0) {
-            // at least one unit per resident warp, and segments of at most 8192
-            // steps so long sequences split into many small balanced units
+            // about one unit per resident warp (one segment fewer when that
+            // still fills 95 % of them: the output pass then runs in one wave,
+            // not 1.3), and segments of at most 8192 steps so long sequences
+            // split into many small balanced units
             const long long rb = ssh::pair_row_blocks(p);
             long long r = (resident + rb - 1) / rb;
+            if (r > 2 && rb * (r - 1) * 20 >= resident * 19) --r;
             const long long by_len = (p.seqlen + 8191) / 8192;
             if (by_len > r) r = by_len;
             req = (int)(r < 2 ? 2 : (r > 65535 ? 65535 : r));
