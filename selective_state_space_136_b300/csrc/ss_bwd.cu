@@ -749,6 +749,28 @@ __global__ void __launch_bounds__(64, 9) scan_bwd_split_kernel(const ssh::BwdPar
         const float2 v = *reinterpret_cast<const float2 *>(&sm.bc[t][N + n0 + 2 * j]);
         return mk2(v.x, v.y);
     };
+    // 8 terms per lane (this lane's states) summed over the warp's 16 rows (the
+    // lanes of one q): halving exchanges over lane bits 4..2 leave each lane with
+    // value (lane >> 2) of its half summed over 8 rows, one more exchange over
+    // bit 1 completes the sum, and the lanes with bit 1 clear add it to dst
+    // (state n0 + value) at step l
+    auto step_sum8 = [&](float (&v)[8], float *dst, long long l) {
+#pragma unroll
+        for (int m = 16, c = 8; m >= 4; m >>= 1, c >>= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int i = 0; i < c / 2; ++i) {
+                const float send = upper ? v[i] : v[i + c / 2];
+                const float keep = upper ? v[i + c / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(FULL, send, m);
+            }
+        }
+        const float tot = v[0] + __shfl_xor_sync(FULL, v[0], 2);
+        if ((lane & 2) == 0) {
+            const int i = lane >> 2;  // value index: 4 bit4 + 2 bit3 + bit2
+            atomicAdd(dst + ((long long)b * N + n0 + i) * L + l, tot);
+        }
+    };
     // one forward step of this lane's states; du is dt * u (simplified) or u (zero-order hold)
     auto fwd_step = [&](f2 *h, float dt, float du, int t) {
         const float dl = dt * kLog2e;
@@ -888,16 +910,25 @@ __global__ void __launch_bounds__(64, 9) scan_bwd_split_kernel(const ssh::BwdPar
                 gD = fmaf(gs, u, gD);
                 const float dl = dtt * kLog2e;
                 const f2 gs2 = mk2(gs, gs), dd = mk2(dtt, dtt), dd2 = mk2(dl, dl), uu = mk2(u, u);
+                // dC of the step (gs h) summed over the warp's 16 rows before the
+                // pair loop, so only the 8 dB terms are alive after it
+                {
+                    float c8[8];
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) {
+                        const f2 vc = fmul2(gs2, hcur[j]);
+                        c8[2 * j] = vc.x, c8[2 * j + 1] = vc.y;
+                    }
+                    step_sum8(c8, p.dC, l0 + tt);
+                }
                 f2 gu2 = mk2(0.f, 0.f), gdt2 = mk2(0.f, 0.f);
-                float v[16];  // this lane's dB (i < 8) and dC (i >= 8) terms of the step
+                float v[8];  // this lane's dB terms of the step
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
                     const f2 Bp = Bpair(tt, j), Cp = Cpair(tt, j);
                     const f2 tq = fmul2(dd2, Ar[j]);
                     const f2 e = mk2(ex2(tq.x), ex2(tq.y));
                     g[j] = ffma2(gs2, Cp, g[j]);
-                    const f2 vc = fmul2(gs2, hcur[j]);
-                    v[8 + 2 * j] = vc.x, v[8 + 2 * j + 1] = vc.y;
                     const f2 ehp = fmul2(e, hprev[j]);
                     if constexpr (ZH) {
                         f2 fa;
@@ -933,24 +964,7 @@ __global__ void __launch_bounds__(64, 9) scan_bwd_split_kernel(const ssh::BwdPar
                     wm.io[1][tt][rr] = gu_;
                     wm.io[0][tt][rr] = gx;
                 }
-                // dB and dC of the step summed over the warp's 16 rows (lanes of
-                // one q): halving exchanges over lane bits 4..1; lane 2 i + q
-                // ends with value i of its half
-#pragma unroll
-                for (int m = 16, c = 16; m >= 2; m >>= 1, c >>= 1) {
-                    const bool upper = (lane & m) != 0;
-#pragma unroll
-                    for (int i = 0; i < c / 2; ++i) {
-                        const float send = upper ? v[i] : v[i + c / 2];
-                        const float keep = upper ? v[i + c / 2] : v[i];
-                        v[i] = keep + __shfl_xor_sync(FULL, send, m);
-                    }
-                }
-                {
-                    const int i = rr;  // value index held by this lane
-                    float *dst = (i < 8 ? p.dB : p.dC) + ((long long)b * N + n0 + (i & 7)) * L + l0 + tt;
-                    atomicAdd(dst, v[0]);
-                }
+                step_sum8(v, p.dB, l0 + tt);
             }
             __syncwarp();
         }
