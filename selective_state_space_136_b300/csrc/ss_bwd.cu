@@ -28,7 +28,8 @@
 // once per row at the end.
 //
 // Layout: one warp per row block (32 channels of one batch), one thread per
-// row with all N states in registers.
+// row with all N states in registers; for dstate 16 with the zero-order hold,
+// a CTA of two warps per row block with a row's states over two lanes.
 #include "ss_common.cuh"
 #include "ss_internal.h"
 
