@@ -68,6 +68,7 @@ struct TcSmem {
     float cum[kQ];
     float W[kQ];  // exp2(cum_e - cum_s) dt_s, e the last step of s's 16-column block
     uint64_t bar;      // G of the chunk done
+    uint64_t bars;     // Z and S of the chunk done (committed after S)
     uint64_t bary;     // every product of the chunk done (committed after Y)
     uint64_t bardrain; // after a wait that gave up: whatever was issued is done
     uint64_t cbar[2];  // TMA arrival of C and B into buffer 0 / 1
@@ -410,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
+        mbar_init(&sm.bars, 1);
         mbar_init(&sm.bary, 1);
         mbar_init(&sm.bardrain, 1);
         mbar_init(&sm.cbar[0], 1);
@@ -557,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < kQ / 16; ++k)
                     mma_f16(tmem + kColS, dadv(dBt, k * kMn128Step), dadv(dXs, k * kMn64Step), kIdS, true);
+                mma_commit(&sm.bars);
             }
             __syncwarp();
         }
@@ -630,7 +633,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // meanwhile: the next chunk's dt, running sum and block weights (its raw
         // dt was loaded at this chunk's start)
         if (warp == 0 && more) dt_scan(dr, nd, nc, nw);
-        if (__syncthreads_or(!mma_wait(&sm.bary, phase, p.wait_limit))) {
+        // meanwhile too: the new state's row n = r (this part's columns) into H
+        // for the next chunk's Z; Z and S are done (this chunk's Z has read H)
+        const bool s_ok = mma_wait(&sm.bars, phase, p.wait_limit);
+        if (s_ok) {
+            tc_fence_after();
+            const int n = r;
+#pragma unroll
+            for (int j = 0; j < kCols / 16; ++j) {
+                float v0[16];
+                tmem_ld16(trow + kColS + c0 + 16 * j, v0);
+                put_state16(sH, n, c0 + 16 * j, v0);
+            }
+        }
+        if (__syncthreads_or(!s_ok || !mma_wait(&sm.bary, phase, p.wait_limit))) {
             if (tid == 0) set_error(p.err, SS_ERR_TIMEOUT);
             timed_out = true;
             break;
@@ -639,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 
         // ---- y row t = r, this part's channels, into the staging tile (the M
-        // buffer) and out by TMA; the new state's row n = r (same columns) into H
+        // buffer) and out by TMA
         {
             const int t = r;
             const float ft = ex2(sm.cum[t]);
@@ -661,9 +677,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld16x3(trow + kColY + c0 + 16 * j, trow + kColZ + c0 + 16 * j,
                             trow + kColZ + kP + c0 + 16 * j, y0, zh0, zl0);
                 finish(j, y0, zh0, zl0);
-                float v0[16];
-                tmem_ld16(trow + kColS + c0 + 16 * j, v0);
-                put_state16(sH, t, c0 + 16 * j, v0);
             }
         }
         fence_proxy_async();  // the staged y is visible to the TMA unit
