@@ -41,7 +41,7 @@
 #define SS_PAIR_TL 16
 #endif
 #ifndef SS_PAIR_S
-#define SS_PAIR_S 3
+#define SS_PAIR_S 4
 #endif
 #ifndef SS_PAIR_MINB
 #define SS_PAIR_MINB 8
